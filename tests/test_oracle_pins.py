@@ -1,0 +1,317 @@
+"""Pins of the CPU oracle to things other than itself (CPU only).
+
+Each test checks the oracle against what the pages or mathematics fix:
+worked numbers from the pages, exact invariants of the shard layout, closed
+forms, special cases that reduce to a library routine, and brute force on
+tiny inputs.  A plausible slip in the oracle (dropped term, wrong sign or
+index, transposed operand) fails at least one of them.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import synthetic
+from oracle import dit, shards
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------
+# Shard layout ("vLLM-Omni 发布 Distributed Layerwise Offload…", section 2)
+# ----------------------------------------------------------------------------
+
+def test_shards_brute_force_small():
+    """Every n <= 40, dp <= 9: equal shard length, zero padding, exact reassembly."""
+    for n in range(0, 41):
+        flat = np.arange(1, n + 1, dtype=np.uint16)  # nonzero payload
+        for dp in range(1, 10):
+            sh = shards.pack(flat, dp)
+            S = shards.shard_numel(n, dp)
+            assert len(sh) == dp
+            assert all(s.size == S for s in sh)
+            assert S * dp >= n and S * dp - n < dp
+            if n:
+                assert (S - 1) * dp < n  # smallest equal length that holds n
+            g = shards.gather(sh)
+            assert np.array_equal(g[:n], flat)
+            assert not g[n:].any()
+            # rank r holds exactly flat[r*S : (r+1)*S]
+            for r in range(dp):
+                lo, hi = min(r * S, n), min((r + 1) * S, n)
+                assert np.array_equal(sh[r][: hi - lo], flat[lo:hi])
+
+
+def test_shards_entirely_padding():
+    """n=5, dp=8: S=1, ranks 5..7 hold only padding."""
+    sh = shards.pack(np.array([7, 7, 7, 7, 7], np.uint16), 8)
+    assert [int(s[0]) for s in sh] == [7, 7, 7, 7, 7, 0, 0, 0]
+
+
+def test_shards_bit_exact_on_nan_payloads():
+    """Packing moves raw bits: NaN/Inf/-0 bf16 patterns survive unchanged."""
+    flat = np.array([0x7FC1, 0xFF80, 0x8000, 0x0001, 0x7F80, 0x1234, 0xFFFF], np.uint16)
+    for dp in range(1, 9):
+        assert np.array_equal(shards.unpack(shards.pack(flat, dp), flat.size), flat)
+
+
+def test_golden_shard_sizes_from_pages():
+    """The pages' worked per-rank sizes: 124 GB / DP4 -> 31 GB, 29 GB / DP2 -> 14.5 GB."""
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "shard_sizes.txt"))
+            if l.strip() and not l.startswith("#")]
+    assert len(rows) >= 2
+    for total_bytes, dp, per_rank, _src in rows:
+        n_elem = int(total_bytes) // 2
+        S = shards.shard_numel(n_elem, int(dp))
+        assert S * 2 == int(per_rank)
+        # total pinned over all ranks is the model size, not dp x model size
+        assert S * int(dp) * 2 - int(total_bytes) < int(dp) * 2
+
+
+def test_views_repoint_into_gathered_buffer():
+    h, m, C = 16, 64, 8
+    table = dit.param_table(h, m, C)
+    n = dit.block_numel(h, m, C)
+    flat = synthetic.normal_bf16_bits(3, 77, (n,), 0.02)
+    for dp in (1, 3, 4, 7):
+        g = shards.gather(shards.pack(flat, dp))
+        v = shards.views(g, table)
+        off = 0
+        for name, shape in dit.param_shapes(h, m, C):
+            k = int(np.prod(shape))
+            assert v[name].shape == shape
+            assert np.array_equal(v[name].reshape(-1), flat[off:off + k])
+            off += k
+
+
+def test_block_numel_closed_form_and_workload_sizes():
+    """n = 6hC + 6h + 4h^2 + 4h + 2hm + m + h, and the workloads' stated sizes."""
+    for cfg in synthetic.CONFIGS.values():
+        h, m, C = cfg.hidden, cfg.mlp, cfg.cond_dim
+        n = dit.block_numel(h, m, C)
+        assert n == 6 * h * C + 6 * h + 4 * h * h + 4 * h + 2 * h * m + m + h
+    # "~3.2B params, ~6.4 GB" (deep), "~12.6B params, ~25 GB" (video),
+    # "~1.6 GB bf16 per block, ~39 GB host" (large): within the 2.5% that the
+    # per-block 256 -> 6h modulation linear adds over 12 h^2 per block.
+    deep, video, large = (synthetic.CONFIGS[k] for k in ("deep", "video", "large"))
+    tot = lambda c: c.blocks * dit.block_numel(c.hidden, c.mlp, c.cond_dim)
+    assert abs(tot(deep) / 3.2e9 - 1) < 0.035
+    assert abs(tot(video) / 12.6e9 - 1) < 0.035
+    assert abs(dit.block_numel(large.hidden, large.mlp, large.cond_dim) * 2 / 1.6e9 - 1) < 0.035
+    assert abs(tot(large) * 2 / 39e9 - 1) < 0.035
+
+
+# ----------------------------------------------------------------------------
+# Generator (input recipe; pinned to the published splitmix64 definition)
+# ----------------------------------------------------------------------------
+
+def _splitmix64_sequential(state, count):
+    M = (1 << 64) - 1
+    out = []
+    for _ in range(count):
+        state = (state + 0x9E3779B97F4A7C15) & M
+        z = state
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & M
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & M
+        out.append(z ^ (z >> 31))
+    return out
+
+
+def test_generator_matches_sequential_splitmix64():
+    M = (1 << 64) - 1
+
+    def mix(z):
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & M
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & M
+        return z ^ (z >> 31)
+
+    for seed, tid in ((0, 0), (1, 5), (12345, 0xF0000001)):
+        s = mix(seed ^ mix((tid + 0x9E3779B97F4A7C15) & M))
+        want = _splitmix64_sequential(s, 64)
+        got = synthetic.raw_u64(seed, tid, 64)
+        assert [int(v) for v in got] == want
+
+
+def test_generator_bf16_rounding_matches_torch_rne():
+    f = synthetic.normal_f32(0, 9, (100000,), 0.02)
+    b = synthetic.normal_bf16_bits(0, 9, (100000,), 0.02)
+    tb = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(b, tb)
+
+
+def test_generator_moments():
+    z = synthetic.normal_f32(0, 11, (1 << 20,), 1.0).astype(np.float64)
+    assert abs(z.mean()) < 5e-3 and abs(z.std() - 1) < 5e-3
+    assert abs((z ** 4).mean() - 3) < 0.05  # Gaussian kurtosis
+
+
+# ----------------------------------------------------------------------------
+# Block math pins
+# ----------------------------------------------------------------------------
+
+def _rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+def test_layer_norm_matches_torch_and_closed_forms():
+    x = _rng(1).normal(size=(7, 96)) * 3 + 1.5
+    want = F.layer_norm(torch.from_numpy(x), (96,), eps=1e-6).numpy()
+    np.testing.assert_allclose(dit.layer_norm(x), want, rtol=1e-12, atol=1e-12)
+    # constant rows normalise to exactly zero, so modulate gives exactly shift
+    c = np.full((3, 32), 2.75)
+    shift, scale = _rng(2).normal(size=32), _rng(3).normal(size=32)
+    assert not dit.layer_norm(c).any()
+    assert np.array_equal(dit.modulate(dit.layer_norm(c), shift, scale), np.broadcast_to(shift, (3, 32)))
+    # affine invariance LN(a x + b) = LN(x) up to eps
+    np.testing.assert_allclose(dit.layer_norm(4 * x + 9), dit.layer_norm(x), atol=1e-6)
+
+
+def test_gelu_and_silu_match_torch():
+    v = np.linspace(-8, 8, 2001)
+    np.testing.assert_allclose(dit.gelu_tanh(v), F.gelu(torch.from_numpy(v), approximate="tanh").numpy(),
+                               rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(dit.silu(v), F.silu(torch.from_numpy(v)).numpy(), rtol=1e-13, atol=1e-15)
+    assert dit.gelu_tanh(np.array([0.0]))[0] == 0.0
+
+
+def test_linear_orientation_matches_torch_linear():
+    u, w, b = _rng(4).normal(size=(5, 12)), _rng(5).normal(size=(7, 12)), _rng(6).normal(size=7)
+    want = F.linear(torch.from_numpy(u), torch.from_numpy(w), torch.from_numpy(b)).numpy()
+    np.testing.assert_allclose(dit.linear(u, w, b), want, rtol=1e-13, atol=1e-13)
+
+
+@pytest.mark.parametrize("T,H,d", [(1, 2, 8), (5, 1, 16), (33, 3, 8), (130, 2, 64)])
+def test_attention_matches_torch_sdpa(T, H, d):
+    rng = _rng(T * 7 + d)
+    q, k, v = (rng.normal(size=(T, H * d)) * 1.5 for _ in range(3))
+    got = dit.attention(q, k, v, H)
+    th = lambda a: torch.from_numpy(a).reshape(T, H, d).permute(1, 0, 2)[None]
+    want = F.scaled_dot_product_attention(th(q), th(k), th(v))[0].permute(1, 0, 2).reshape(T, H * d).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    rng = _rng(8)
+    H, d, T = 2, 16, 9
+    v = rng.normal(size=(T, H * d))
+    # one token: the softmax weight is exactly 1, output is v
+    q1, k1, v1 = rng.normal(size=(1, H * d)), rng.normal(size=(1, H * d)), rng.normal(size=(1, H * d))
+    assert np.array_equal(dit.attention(q1, k1, v1, H), v1)
+    # zero queries: uniform weights, output is the column mean of v
+    out = dit.attention(np.zeros((T, H * d)), rng.normal(size=(T, H * d)), v, H)
+    np.testing.assert_allclose(out, np.broadcast_to(v.mean(0), (T, H * d)), rtol=1e-12, atol=1e-13)
+    # one key much larger than the rest: output is that key's value row
+    k = np.zeros((T, H * d)); k[4] = 50.0
+    q = np.ones((T, H * d))
+    np.testing.assert_allclose(dit.attention(q, k, v, H), np.broadcast_to(v[4], (T, H * d)), atol=1e-12)
+
+
+def test_attention_head_columns_and_permutations():
+    rng = _rng(9)
+    H, d, T = 3, 8, 11
+    q, k, v = (rng.normal(size=(T, H * d)) for _ in range(3))
+    base = dit.attention(q, k, v, H)
+    # perturbing head 2's columns leaves heads 0 and 1 unchanged
+    k2 = k.copy(); k2[:, 2 * d:] += rng.normal(size=(T, d))
+    out = dit.attention(q, k2, v, H)
+    assert np.array_equal(out[:, :2 * d], base[:, :2 * d])
+    assert not np.allclose(out[:, 2 * d:], base[:, 2 * d:])
+    # adding one vector to every key shifts each logit row by a constant:
+    # softmax is shift invariant, so nothing changes
+    k3 = k + rng.normal(size=(1, H * d))
+    np.testing.assert_allclose(dit.attention(q, k3, v, H), base, rtol=1e-11, atol=1e-12)
+    # joint permutation of keys and values changes nothing; queries permute
+    perm = rng.permutation(T)
+    np.testing.assert_allclose(dit.attention(q, k[perm], v[perm], H), base, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dit.attention(q[perm], k, v, H), base[perm], rtol=1e-12, atol=1e-13)
+
+
+def _tiny_params(h=32, m=64, C=16, seed=0, std=0.3):
+    rng = _rng(seed)
+    return {name: rng.normal(size=shape) * std for name, shape in dit.param_shapes(h, m, C)}
+
+
+def test_adaln_zero_weight_gives_bias_and_split_order():
+    h, C = 8, 4
+    b = np.arange(6 * h, dtype=np.float64)
+    mod = dit.adaln_modulation(np.zeros((6 * h, C)), b, _rng(1).normal(size=(2, C)))
+    assert np.array_equal(mod, np.broadcast_to(b, (2, 6 * h)))
+    parts = dit.split_modulation(mod, h)
+    for i, p in enumerate(parts):
+        assert np.array_equal(p[0], b[i * h:(i + 1) * h])
+
+
+def test_block_zero_gates_is_identity():
+    """ada_w = 0 and the gate entries of ada_b = 0 make the block exactly the identity."""
+    h, m, C, H = 32, 64, 16, 2
+    p = _tiny_params(h, m, C)
+    p["ada_w"] = np.zeros_like(p["ada_w"])
+    p["ada_b"][2 * h:3 * h] = 0.0
+    p["ada_b"][5 * h:6 * h] = 0.0
+    x = _rng(3).normal(size=(2, 7, h))
+    c = _rng(4).normal(size=(2, C))
+    assert np.array_equal(dit.block_forward(x, c, p, H), x)
+
+
+def test_block_matches_torch_module_assembly():
+    """A block built from torch.nn.functional library routines agrees to 1e-12."""
+    h, m, C, H = 32, 96, 16, 4
+    p = _tiny_params(h, m, C, std=0.2)
+    x = _rng(5).normal(size=(2, 13, h))
+    c = _rng(6).normal(size=(2, C))
+    got = dit.block_forward(x, c, p, H)
+
+    tp = {k: torch.from_numpy(v) for k, v in p.items()}
+    tx, tc = torch.from_numpy(x), torch.from_numpy(c)
+    mod = F.linear(F.silu(tc), tp["ada_w"], tp["ada_b"])
+    sh1, sc1, g1, sh2, sc2, g2 = (t[:, None, :] for t in mod.chunk(6, dim=-1))
+    u = F.layer_norm(tx, (h,), eps=1e-6) * (1 + sc1) + sh1
+    q, k, v = F.linear(u, tp["qkv_w"], tp["qkv_b"]).chunk(3, dim=-1)
+    heads = lambda t: t.reshape(2, 13, H, h // H).transpose(1, 2)
+    o = F.scaled_dot_product_attention(heads(q), heads(k), heads(v)).transpose(1, 2).reshape(2, 13, h)
+    x1 = tx + g1 * F.linear(o, tp["proj_w"], tp["proj_b"])
+    u2 = F.layer_norm(x1, (h,), eps=1e-6) * (1 + sc2) + sh2
+    want = x1 + g2 * F.linear(F.gelu(F.linear(u2, tp["fc1_w"], tp["fc1_b"]), approximate="tanh"),
+                              tp["fc2_w"], tp["fc2_b"])
+    np.testing.assert_allclose(got, want.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_block_rows_equals_full_block():
+    h, m, C, H = 32, 64, 16, 2
+    p = _tiny_params(h, m, C, std=0.2)
+    x = _rng(7).normal(size=(3, 17, h))
+    c = _rng(8).normal(size=(3, C))
+    full = dit.block_forward(x, c, p, H)
+    rows = np.array([0, 5, 16])
+    for r in range(3):
+        np.testing.assert_allclose(dit.block_forward_rows(x, c, p, H, r, rows), full[r, rows],
+                                   rtol=1e-12, atol=1e-13)
+
+
+def test_requests_are_independent():
+    h, m, C, H = 32, 64, 16, 2
+    p = _tiny_params(h, m, C, std=0.2)
+    x = _rng(9).normal(size=(2, 6, h))
+    c = _rng(10).normal(size=(2, C))
+    both = dit.block_forward(x, c, p, H)
+    one = dit.block_forward(x[1:], c[1:], p, H)
+    # equal up to rounding: BLAS may order a 1-row product differently
+    np.testing.assert_allclose(both[1:], one, rtol=1e-13, atol=1e-14)
+    x2 = x.copy(); x2[0] += 1.0  # changing request 0 leaves request 1 alone
+    np.testing.assert_allclose(dit.block_forward(x2, c, p, H)[1], both[1], rtol=1e-13, atol=1e-14)
+
+
+def test_streamed_equals_resident_and_dp_invariant_on_oracle():
+    """Placement never changes the math: params re-pointed from gathered shards
+    give bit-identical outputs for every dp (the pages' identical-hash check)."""
+    h, m, C, H = 32, 64, 16, 2
+    n = dit.block_numel(h, m, C)
+    flats = [synthetic.weight_bits(0, b, 0, (n,)) for b in range(3)]
+    x = synthetic.tokens(0, 1, 9, h)
+    c = synthetic.cond(0, 1, C)
+    ref = dit.forward(x, c, [dit.params_from_flat(f, h, m, C) for f in flats], H)
+    for dp in (1, 2, 3, 4, 8):
+        blocks = [dit.params_from_flat(shards.unpack(shards.pack(f, dp), n), h, m, C) for f in flats]
+        assert np.array_equal(dit.forward(x, c, blocks, H), ref)
