@@ -1,0 +1,350 @@
+"""Benchmark of the layerwise weight-streaming DiT forward on GB300.
+
+One step = one streamed forward over all blocks of the workload (every
+kernel of every block plus the slot fills), inputs resident in HBM.  Prints
+ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload t2i]
+    python bench.py --impl reference      # the CPU oracle as the reference arm
+
+Metric: DiT tokens/s with streamed weights (R*T per forward / forward time),
+plus block-forwards/s, and the per-block roofline fraction
+sum_b max(bytes_b / H2D GB/s, flops_b / tensor peak) / measured time.
+Multi-GPU (torchrun): replicas only - every rank streams its own copy of the
+workload on its own GPU, no collective on the data path; value = all tokens /
+max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DiT tokens/s with streamed weights; % of max(host-link, tensor-core) roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="t2i", help="tiny | t2i | deep | video | large")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--fill", default="auto", choices=["auto", "memcpy", "zerocopy"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-profile", action="store_true", help="no per-kernel events in the timed region")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    return ap.parse_args()
+
+
+def block_flops(cfg, R, T):
+    """Dense contraction FLOPs of one block (tensor-core work only)."""
+    h, m, C = cfg.hidden, cfg.mlp, cfg.cond_dim
+    M = R * T
+    gemm = 2 * M * (3 * h * h + h * h + 2 * h * m)
+    attn = 4 * R * T * T * h
+    ada = 12 * R * C * h
+    return gemm, attn, ada
+
+
+def kernel_flops(cfg, R, T):
+    h, m = cfg.hidden, cfg.mlp
+    M = R * T
+    return {"gemm_qkv": 2 * M * 3 * h * h, "gemm_proj": 2 * M * h * h, "gemm_fc1": 2 * M * h * m,
+            "gemm_fc2": 2 * M * m * h, "attention": 4 * R * T * T * h}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_info():
+    model = ""
+    try:
+        for l in open("/proc/cpuinfo"):
+            if l.lower().startswith(("model name", "cpu part")):
+                model = l.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return os.cpu_count(), model
+
+
+def oracle_block_time(cfg, seed=0, blocks=1):
+    """Times the CPU oracle on `blocks` blocks of the workload (all R*T tokens)."""
+    import synthetic
+    from oracle import dit
+    params = []
+    for b in range(blocks):
+        params.append({name: dit.bf16_to_f64(synthetic.weight_bits(seed, b, i, shape)).reshape(shape)
+                       for i, (name, shape) in enumerate(dit.param_shapes(cfg.hidden, cfg.mlp, cfg.cond_dim))})
+    x = synthetic.tokens(seed, cfg.requests, cfg.tokens, cfg.hidden)
+    c = synthetic.cond(seed, cfg.requests, cfg.cond_dim)
+    t0 = time.perf_counter()
+    dit.forward(x, c, params, cfg.heads)
+    return (time.perf_counter() - t0) / blocks
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        return max((p.get("num_threads", 1) for p in threadpool_info()), default=os.cpu_count())
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, cfg, rank, world):
+    """The reference arm: the CPU oracle as it stands, rank 0 only."""
+    if rank != 0:
+        return
+    tokens = cfg.requests * cfg.tokens
+    for _ in range(args.warmup):
+        oracle_block_time(cfg)
+    times = [oracle_block_time(cfg) for _ in range(args.steps)]
+    per_block = float(np.mean(times))
+    step_s = per_block * cfg.blocks
+    value = tokens / step_s
+    cores, model = cpu_info()
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.describe(), "global_batch": cfg.requests, "seq_len": cfg.tokens,
+                   "parallelism": "cpu"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": f"each step = 1 of {cfg.blocks} blocks over all {tokens} tokens, "
+                                   f"x{cfg.blocks} extrapolated; cpu {model}"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    import synthetic
+    cfg = synthetic.get_config(args.workload)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, cfg, rank, world)
+
+    import torch
+    import layerwise_weight_offloaded_gb300 as dlo
+    from layerwise_weight_offloaded_gb300 import build as dlo_build
+    from layerwise_weight_offloaded_gb300.pinned import PinnedShards
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dlo_build.build()
+    dev = torch.cuda.current_device()
+
+    R, T, L, dp = cfg.requests, cfg.tokens, cfg.blocks, cfg.dp_size
+    spec = (cfg.hidden, cfg.heads, cfg.mlp, cfg.cond_dim)
+    specs = [spec] * L
+    ps = PinnedShards(specs, dp, lambda b, i, shape: synthetic.weight_bits(cfg.seed, b, i, shape))
+    fill = {"auto": dlo.DLO_FILL_AUTO, "memcpy": dlo.DLO_FILL_MEMCPY, "zerocopy": dlo.DLO_FILL_ZEROCOPY}[args.fill]
+    profile = not args.no_profile
+    h = dlo.dlo_create(specs, dp, ps.ptrs, fill | (dlo.DLO_PROFILE if profile else 0))
+    st0 = dlo.dlo_get_stats(h)
+
+    x0 = torch.from_numpy(synthetic.tokens(cfg.seed, R, T, cfg.hidden)).cuda()
+    cond = torch.from_numpy(synthetic.cond(cfg.seed, R, cfg.cond_dim)).cuda()
+    x = x0.clone()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # > 129 MB L2
+
+    for _ in range(args.warmup):
+        x.copy_(x0)
+        dlo.dlo_forward(h, x, cond, R, T, stream)
+    dlo.dlo_synchronize(h, 600000)
+    torch.cuda.synchronize()
+
+    kclasses = dlo.KERNEL_CLASSES
+    ktime = {k: 0.0 for k in kclasses}
+    klaunch = {k: 0 for k in kclasses}
+    launches0 = dlo.dlo_get_stats(h)["kernel_launches"]
+    clocks = ClockSampler(dev)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    total_ms = 0.0
+    for _ in range(args.steps):
+        x.copy_(x0)
+        flush.fill_(1)  # evict L2 between steps (outside the timed events)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dlo.dlo_forward(h, x, cond, R, T, stream)
+        b.record(stream)
+        b.synchronize()
+        total_ms += a.elapsed_time(b)
+        if profile:
+            for k, (ms, n) in dlo.dlo_get_kernel_times(h).items():
+                ktime[k] += ms
+                klaunch[k] += n
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    dlo.dlo_synchronize(h, 600000)
+    launches = dlo.dlo_get_stats(h)["kernel_launches"] - launches0
+    ms_step = total_ms / args.steps
+    if dist:
+        t = torch.tensor([ms_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    tokens = R * T
+    value = tokens * world / (ms_step * 1e-3)
+
+    # end to end through the public API from host buffers (H2D + forward + D2H timed)
+    xh = torch.from_numpy(synthetic.tokens(cfg.seed, R, T, cfg.hidden)).pin_memory()
+    ch = torch.from_numpy(synthetic.cond(cfg.seed, R, cfg.cond_dim)).pin_memory()
+    dlo.dlo_forward_host(h, xh, ch, R, T, stream)  # warm the staging buffers
+    e2e_s = []
+    for _ in range(args.e2e_steps):
+        xh.copy_(torch.from_numpy(synthetic.tokens(cfg.seed, R, T, cfg.hidden)))
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dlo.dlo_forward_host(h, xh, ch, R, T, stream)
+        e2e_s.append(time.perf_counter() - t0)
+    e2e_step = float(np.mean(e2e_s))
+    if dist:
+        t = torch.tensor([e2e_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_step = float(t.item())
+    st = dlo.dlo_get_stats(h)
+
+    peaks, peak_src = measured_peaks()
+    p_tc = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * 1e12
+    bw = max(st["h2d_memcpy_gbs"], st["h2d_zerocopy_gbs"]) * 1e9
+    if bw <= 0:
+        bw = float("nan")
+    gemm_f, attn_f, ada_f = block_flops(cfg, R, T)
+    block_bytes = st["slot_bytes"]  # dp * S * 2 algorithmic bytes over the host link per block
+    roof_block_s = max(block_bytes / bw, (gemm_f + attn_f + ada_f) / p_tc)
+    path_frac = roof_block_s * L / (ms_step * 1e-3)
+
+    roofline = None
+    if profile:
+        kf = kernel_flops(cfg, R, T)
+        dom = max(kf, key=lambda k: ktime[k])
+        per_launch_s = ktime[dom] / max(klaunch[dom], 1) * 1e-3
+        achieved = kf[dom] / per_launch_s / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved,
+                    "peak": p_tc / 1e12, "unit": "TFLOP/s", "frac": achieved / (p_tc / 1e12),
+                    "traffic": None,
+                    "peak_source": f"bf16_tflops_sustained of {peak_src} peaks (kernel timed inside a long step)",
+                    "per_kernel_ms_per_step": {k: ktime[k] / args.steps for k in kclasses},
+                    "per_kernel_tflops": {k: kf[k] / (ktime[k] / max(klaunch[k], 1) * 1e-3) / 1e12
+                                          for k in kf if ktime[k] > 0}}
+
+    cpu_base = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        per_block = oracle_block_time(cfg)
+        cpu_base = {"value": tokens / (per_block * L), "unit": "tokens/s", "cores": blas_threads(),
+                    "kind": "oracle", "sample": f"1 of {L} blocks over all {tokens} tokens, float64, "
+                                                f"x{L} extrapolated ({per_block:.2f} s/block); cpu {cpu_info()[1]}"}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.describe(), "global_batch": R * world, "seq_len": T,
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": "flushed between steps (256 MB write)", "fill": args.fill},
+        "block_forwards_per_s": L * world / (ms_step * 1e-3),
+        "path_roofline": {"frac": path_frac, "per_block_roofline_ms": roof_block_s * 1e3,
+                          "bound": "host-link" if block_bytes / bw > (gemm_f + attn_f + ada_f) / p_tc else "tensor",
+                          "h2d_gbs_measured": bw / 1e9, "block_bytes": block_bytes,
+                          "block_flops": gemm_f + attn_f + ada_f, "tensor_peak_tflops": p_tc / 1e12},
+        "roofline": roofline,
+        "cpu_baseline": cpu_base,
+        "e2e": {"value": tokens * world / e2e_step, "unit": "tokens/s",
+                "h2d_bytes_per_step": xh.numel() * 4 + ch.numel() * 4, "d2h_bytes_per_step": xh.numel() * 4},
+        "gpu_launches": launches,
+        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "weights": {"fill_mode": {1: "memcpy", 2: "zerocopy"}.get(st["fill_mode"]),
+                    "h2d_memcpy_gbs": st["h2d_memcpy_gbs"], "h2d_zerocopy_gbs": st["h2d_zerocopy_gbs"],
+                    "device_weight_bytes": st["device_weight_high_water"], "slot_bytes": st["slot_bytes"],
+                    "host_shard_bytes": st["host_shard_bytes"]},
+    }
+    dlo.dlo_destroy(h)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

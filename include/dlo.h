@@ -1,0 +1,276 @@
+/*
+ * dlo.h - C ABI of the layerwise weight-streaming DiT forward on one GB300.
+ *
+ * Source of the method: "vLLM-Omni 发布 Distributed Layerwise Offload，支持
+ * 200B+ DiT 模型多卡部署" (aisignalhub.me write-up), below "the write-up":
+ *   section 2  "weight sharding with AllGather reconstruction": each rank keeps
+ *              1/dp_size of every layer as an equal, ceil-divided, zero-padded
+ *              flat shard in pinned host memory; the full layer is rebuilt by an
+ *              all-gather of the shards;
+ *   section 3  "double-buffered prefetch with H2D + AllGather overlap": exactly
+ *              two device slots, each as large as the largest block; a copy
+ *              stream prepares block N+1 in one slot while the compute stream
+ *              runs block N from the other, ordered by events (the three-stream
+ *              timeline figure), so weight HBM stays at 2 x max_block_size
+ *              whatever the depth; parameters are re-pointed to slices of the
+ *              rebuilt buffer from cached metadata.
+ * On one GPU the all-gather becomes a local reassembly: the dp_size shards of
+ * a block are copied back to back into one slot.
+ *
+ * The DiT block itself is not written down by the pages.  This library
+ * computes an adaLN-zero block (names follow the usual DiT notation):
+ *   mod = ada_w . SiLU(c) + ada_b  -> shift1, scale1, gate1, shift2, scale2, gate2
+ *   x  += gate1 * (Attn(LN(x)(1+scale1)+shift1) . proj_w^T + proj_b)
+ *   x  += gate2 * (GELU_tanh((LN(x)(1+scale2)+shift2) . fc1_w^T + fc1_b) . fc2_w^T + fc2_b)
+ * with LN without affine (eps 1e-6), non-causal multi-head softmax attention,
+ * q/k/v = the three h-wide column groups of LN-modulated x . qkv_w^T + qkv_b.
+ *
+ * Conventions for every function:
+ *   - return a dlo_status; nothing is printed and no C++ exception crosses the
+ *     ABI; dlo_last_error() gives a one-line message for the calling thread;
+ *   - "device" pointers are CUDA device memory of the current device, "host"
+ *     pointers are CPU memory; bf16 values travel as uint16_t bit patterns;
+ *   - tensors are dense row-major; sizes are element counts unless stated;
+ *   - a handle that met a CUDA error or a device-side timeout stays in an
+ *     error state: later calls on it return DLO_ERR_STATE (dlo_destroy works).
+ */
+#ifndef DLO_H
+#define DLO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The library is built with hidden visibility; only these declarations are exported. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
+typedef struct CUstream_st* dlo_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    DLO_OK = 0,
+    DLO_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad flag */
+    DLO_ERR_ALIGNMENT = 2,    /* a dimension is not a multiple of 8, or a pointer is misaligned */
+    DLO_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed (see dlo_last_error) */
+    DLO_ERR_OOM = 4,          /* a device or host allocation failed */
+    DLO_ERR_TIMEOUT = 5,      /* dlo_synchronize gave up before the work finished */
+    DLO_ERR_SHAPE = 6,        /* incompatible shapes (e.g. head dim not 64/128, cond widths differ) */
+    DLO_ERR_STATE = 7,        /* the handle is in an error state */
+    DLO_ERR_DEVICE_TIMEOUT = 8,/* a kernel's bounded wait expired; its output is not valid */
+    DLO_ERR_UNSUPPORTED = 9   /* the device is not sm_103 or a mode is unavailable */
+} dlo_status;
+
+/* dlo_create flags. The low two bits select the slot-fill mechanism. */
+enum {
+    DLO_FILL_AUTO = 0,      /* time both mechanisms on block 0 at create and keep the faster */
+    DLO_FILL_MEMCPY = 1,    /* dp_size cudaMemcpyAsync host->device copies (copy engine) */
+    DLO_FILL_ZEROCOPY = 2,  /* shard-gather kernel reading mapped pinned memory, 16-byte loads */
+    DLO_FILL_MASK = 3,
+    DLO_RESIDENT = 1 << 4,  /* copy every block to the device once (no streaming); for checks */
+    DLO_PROFILE = 1 << 5    /* record CUDA events around every kernel (dlo_get_kernel_times) */
+};
+
+/* Shape of one DiT block.  head_dim = hidden / num_heads must be 64 or 128;
+ * hidden, mlp_hidden and cond_dim must be positive multiples of 8 (so every
+ * parameter starts on a 16-byte boundary of the flat buffer); cond_dim <= 1024. */
+typedef struct {
+    int32_t hidden;     /* h */
+    int32_t num_heads;  /* H */
+    int32_t mlp_hidden; /* m */
+    int32_t cond_dim;   /* C: width of the conditioning (timestep) vector */
+} dlo_block_spec;
+
+/* Parameters of a block, in their fixed order in the flat buffer; each is
+ * stored row-major as [out, in] (biases are 1-D). */
+enum {
+    DLO_P_ADA_W = 0,  /* [6h, C] */
+    DLO_P_ADA_B = 1,  /* [6h] */
+    DLO_P_QKV_W = 2,  /* [3h, h] rows: q, then k, then v; head j = rows j*d..(j+1)*d-1 of each */
+    DLO_P_QKV_B = 3,  /* [3h] */
+    DLO_P_PROJ_W = 4, /* [h, h] */
+    DLO_P_PROJ_B = 5, /* [h] */
+    DLO_P_FC1_W = 6,  /* [m, h] */
+    DLO_P_FC1_B = 7,  /* [m] */
+    DLO_P_FC2_W = 8,  /* [h, m] */
+    DLO_P_FC2_B = 9,  /* [h] */
+    DLO_NUM_PARAMS = 10
+};
+
+/* Runtime statistics of a handle (all counters since dlo_create). */
+typedef struct {
+    int64_t num_blocks;
+    int64_t dp_size;
+    int64_t slot_bytes;              /* bytes of ONE weight slot = max_b dp*S_b*2 */
+    int64_t device_weight_bytes;     /* bytes of weight buffers currently allocated on the device */
+    int64_t device_weight_high_water;/* their high-water mark since create */
+    int64_t max_block_bytes;         /* max_b numel_b * 2 (unpadded) */
+    int64_t host_shard_bytes;        /* sum over blocks of dp*S_b*2 */
+    int64_t activation_bytes;        /* device activation scratch currently allocated */
+    int64_t forwards;                /* completed dlo_forward calls */
+    int64_t kernel_launches;         /* kernels launched by this handle */
+    int64_t fills;                   /* slot fills issued */
+    int32_t fill_mode;               /* DLO_FILL_MEMCPY or DLO_FILL_ZEROCOPY, as chosen */
+    int32_t resident;                /* 1 if DLO_RESIDENT */
+    double h2d_memcpy_gbs;           /* measured at create (AUTO) or 0 */
+    double h2d_zerocopy_gbs;         /* measured at create (AUTO) or 0 */
+} dlo_stats;
+
+/* Kernel classes reported by dlo_get_kernel_times. */
+enum {
+    DLO_K_FILL = 0,      /* zero-copy shard gather (0 when the copy engine fills) */
+    DLO_K_ADALN = 1,     /* modulation GEMV */
+    DLO_K_LN_MOD = 2,    /* LayerNorm + modulate (twice per block) */
+    DLO_K_GEMM_QKV = 3,
+    DLO_K_ATTENTION = 4,
+    DLO_K_GEMM_PROJ = 5,
+    DLO_K_GEMM_FC1 = 6,
+    DLO_K_GEMM_FC2 = 7,
+    DLO_K_NUM = 8
+};
+
+/* ---------------- host-only helpers (no GPU needed) ---------------- */
+
+/* Checks a block spec (rules above). */
+int dlo_validate_spec(const dlo_block_spec* spec);
+
+/* *numel = element count of one block's flat buffer
+ *        = 6hC + 6h + 3h^2 + 3h + h^2 + h + 2hm + m + h. */
+int dlo_block_numel(const dlo_block_spec* spec, int64_t* numel);
+
+/* Equal shard length: numel / dp_size rounded up (section 2 of the write-up).
+ * numel >= 0, dp_size >= 1. */
+int dlo_shard_numel(int64_t numel, int32_t dp_size, int64_t* shard_numel);
+
+/* The cached per-parameter metadata of section 3: offsets[i] and numels[i]
+ * (element units, i in the DLO_P_* order) of every parameter inside the
+ * block's flat buffer.  Both arrays must hold DLO_NUM_PARAMS entries. */
+int dlo_param_table(const dlo_block_spec* spec, int64_t* offsets, int64_t* numels);
+
+/* Host packing of one block (section 2): params[i] points at parameter i
+ * (bf16 bits, DLO_P_* order, caller memory); shards[r] (r < dp_size) points
+ * at caller memory of dlo_shard_numel elements each (normally pinned).
+ * Shard r receives flat elements [r*S, (r+1)*S); elements past the end of the
+ * flat buffer are written as zero.  Nothing is allocated. */
+int dlo_pack_block(const dlo_block_spec* spec, const uint16_t* const* params,
+                   int32_t dp_size, uint16_t* const* shards);
+
+/* One-line message describing the last failure on the calling thread. */
+const char* dlo_last_error(void);
+/* Static name of a status code. */
+const char* dlo_status_string(int status);
+
+/* ---------------- streaming runtime ---------------- */
+
+typedef struct dlo_handle dlo_handle;
+
+/* Creates a streaming forward over num_blocks blocks on the current device.
+ *   specs[num_blocks]            block shapes; every block must share cond_dim;
+ *   shard_ptrs[num_blocks*dp]    host pointer of shard r of block b at index
+ *                                b*dp_size + r, each dlo_shard_numel(numel_b, dp)
+ *                                bf16 elements, packed as dlo_pack_block does.
+ * Ownership: the caller owns the shards and must keep them valid and unchanged
+ * until dlo_destroy.  They should be page-locked (cudaHostAlloc or
+ * cudaHostRegister); DLO_FILL_ZEROCOPY and DLO_FILL_AUTO additionally need them
+ * mapped into the device address space (the default for page-locked memory on
+ * this platform) - otherwise DLO_FILL_ZEROCOPY fails with DLO_ERR_INVALID_ARG
+ * and AUTO falls back to the copy engine.
+ * The handle owns the two weight slots (2 x max_b dp*S_b*2 bytes), or with
+ * DLO_RESIDENT one buffer holding every block; the copy stream, events, tensor
+ * maps and the activation scratch (allocated on the first dlo_forward that
+ * needs it, growing with R*T).  Device must be sm_103 (GB300). */
+int dlo_create(const dlo_block_spec* specs, int32_t num_blocks, int32_t dp_size,
+               const void* const* shard_ptrs, uint32_t flags, dlo_handle** out);
+
+/* Runs every block in order over R requests of T tokens, in place:
+ *   x     device fp32 [R, T, hidden] latent tokens (hidden of block 0; all
+ *         blocks must share hidden), overwritten with the output;
+ *   cond  device fp32 [R, cond_dim] conditioning vectors, one per request.
+ * All requests of one call share T (the pages' wave-compatibility rule).
+ * Asynchronous: the work is ordered after prior work on `stream` and the call
+ * returns once it is enqueued (it may allocate activation scratch first).
+ * Weight slots are refilled from the host shards on the handle's copy stream
+ * while the previous block computes.  Concurrent calls on one handle from
+ * several host threads are not supported. */
+int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t num_requests,
+                int32_t tokens_per_request, dlo_stream_t stream);
+
+/* Same forward from HOST buffers: copies x_host [R,T,hidden] and cond_host
+ * [R,cond_dim] to device staging buffers owned by the handle, runs
+ * dlo_forward on `stream`, copies the result back into x_host and waits for
+ * it.  x_host should be page-locked for full speed. */
+int dlo_forward_host(dlo_handle* h, float* x_host, const float* cond_host,
+                     int32_t num_requests, int32_t tokens_per_request, dlo_stream_t stream);
+
+/* Waits up to timeout_ms (< 0: no limit) for all work the handle enqueued;
+ * DLO_ERR_TIMEOUT if it is still running (the handle moves to its error
+ * state), DLO_ERR_DEVICE_TIMEOUT if a kernel reported an expired wait. */
+int dlo_synchronize(dlo_handle* h, int32_t timeout_ms);
+
+int dlo_get_stats(dlo_handle* h, dlo_stats* out);
+
+/* With DLO_PROFILE: per kernel class (DLO_K_*), total device milliseconds and
+ * launches of the most recent dlo_forward.  Synchronises with that forward.
+ * Both arrays hold DLO_K_NUM entries. */
+int dlo_get_kernel_times(dlo_handle* h, double* ms, int64_t* launches);
+
+/* Test access to the slots: fills slot `slot` (0/1) with block `block` on the
+ * copy stream using the handle's fill mechanism, waits, and copies `bytes`
+ * bytes of the slot to host memory dst (bytes <= slot_bytes). */
+int dlo_debug_fill_and_read(dlo_handle* h, int32_t block, int32_t slot, void* dst, int64_t bytes);
+
+/* Releases everything the handle owns (waits for its work first). */
+int dlo_destroy(dlo_handle* h);
+
+/* ---------------- single-op entry points (the kernels of one block) -------------
+ * Each runs one kernel of the block on `stream`, asynchronously, with every
+ * buffer owned by the caller; they exist so each kernel can be checked on its
+ * own.  A kernel whose bounded wait expires sets a device flag that
+ * dlo_op_check() reads, clears and turns into DLO_ERR_DEVICE_TIMEOUT. */
+
+/* mod[R, N] = ada_w[N, C] . SiLU(cond[R, C]) + ada_b[N]   (N = 6h; fp32 out). */
+int dlo_op_adaln(const uint16_t* ada_w, const uint16_t* ada_b, const float* cond,
+                 int32_t R, int32_t C, int32_t N, float* mod, dlo_stream_t stream);
+
+/* u[r*T+t, :] = bf16( LN(x[r*T+t, :]) * (1 + scale[r*mod_stride + :]) + shift[r*mod_stride + :] )
+ * x fp32 [R*T, hidden]; shift/scale fp32 rows of stride mod_stride; u bf16. */
+int dlo_op_ln_modulate(const float* x, const float* shift, const float* scale, int32_t mod_stride,
+                       int32_t R, int32_t T, int32_t hidden, uint16_t* u, dlo_stream_t stream);
+
+/* GEMM epilogues of dlo_op_linear. */
+enum {
+    DLO_EPI_BIAS = 0,          /* out bf16 [M,N] = A.W^T + bias */
+    DLO_EPI_BIAS_GELU = 1,     /* out bf16 [M,N] = GELU_tanh(A.W^T + bias) */
+    DLO_EPI_GATED_RESIDUAL = 2 /* out fp32 [M,N] += gate[(row/T)*gate_stride + col] * (A.W^T + bias) */
+};
+/* A bf16 [M, K] (device, 16-byte aligned), W bf16 [N, K] (16-byte aligned),
+ * bias bf16 [N]; N and K multiples of 8.  tcgen05 tensor cores, fp32
+ * accumulation; T is only used by DLO_EPI_GATED_RESIDUAL. */
+int dlo_op_linear(int32_t epilogue, const uint16_t* A, const uint16_t* W, const uint16_t* bias,
+                  int32_t M, int32_t N, int32_t K, void* out, const float* gate, int32_t gate_stride,
+                  int32_t T, dlo_stream_t stream);
+
+/* Non-causal softmax attention: qkv bf16 [R*T, 3*H*d] (q | k | v column
+ * groups, head j at columns j*d of each), o bf16 [R*T, H*d]; d in {64, 128}. */
+int dlo_op_attention(const uint16_t* qkv, int32_t R, int32_t T, int32_t H, int32_t d,
+                     uint16_t* o, dlo_stream_t stream);
+
+/* Zero-copy shard gather: dst[r*S + i] = shards[r][i] for r < dp, i < S.
+ * shards[] are device-accessible (mapped) pointers; dst device memory. */
+int dlo_op_shard_gather(const uint16_t* const* shards, int32_t dp, int64_t S, uint16_t* dst,
+                        dlo_stream_t stream);
+
+/* Synchronises `stream` and reports (then clears) the single-op timeout flag. */
+int dlo_op_check(dlo_stream_t stream);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DLO_H */

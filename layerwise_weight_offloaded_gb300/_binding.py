@@ -1,0 +1,278 @@
+"""ctypes marshalling for include/dlo.h (see the package docstring)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libdlo.so")
+
+# ---------------------------------------------------------------- constants
+DLO_OK = 0
+DLO_ERR_INVALID_ARG = 1
+DLO_ERR_ALIGNMENT = 2
+DLO_ERR_CUDA = 3
+DLO_ERR_OOM = 4
+DLO_ERR_TIMEOUT = 5
+DLO_ERR_SHAPE = 6
+DLO_ERR_STATE = 7
+DLO_ERR_DEVICE_TIMEOUT = 8
+DLO_ERR_UNSUPPORTED = 9
+
+DLO_FILL_AUTO = 0
+DLO_FILL_MEMCPY = 1
+DLO_FILL_ZEROCOPY = 2
+DLO_RESIDENT = 1 << 4
+DLO_PROFILE = 1 << 5
+
+DLO_NUM_PARAMS = 10
+PARAM_NAMES = ("ada_w", "ada_b", "qkv_w", "qkv_b", "proj_w", "proj_b", "fc1_w", "fc1_b", "fc2_w", "fc2_b")
+
+DLO_EPI_BIAS = 0
+DLO_EPI_BIAS_GELU = 1
+DLO_EPI_GATED_RESIDUAL = 2
+
+KERNEL_CLASSES = ("fill", "adaln", "ln_modulate", "gemm_qkv", "attention", "gemm_proj", "gemm_fc1", "gemm_fc2")
+DLO_K_NUM = len(KERNEL_CLASSES)
+
+# Every symbol include/dlo.h declares (checked by the CPU test suite).
+EXPORTED = (
+    "dlo_validate_spec", "dlo_block_numel", "dlo_shard_numel", "dlo_param_table", "dlo_pack_block",
+    "dlo_last_error", "dlo_status_string", "dlo_create", "dlo_forward", "dlo_forward_host", "dlo_synchronize",
+    "dlo_get_stats", "dlo_get_kernel_times", "dlo_debug_fill_and_read", "dlo_destroy", "dlo_op_adaln",
+    "dlo_op_ln_modulate", "dlo_op_linear", "dlo_op_attention", "dlo_op_shard_gather", "dlo_op_check",
+)
+
+
+class DloLibraryMissing(ImportError):
+    pass
+
+
+class DloError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_name(status)}: {message}")
+        self.status = status
+
+
+class dlo_block_spec(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("mlp_hidden", ctypes.c_int32), ("cond_dim", ctypes.c_int32)]
+
+
+class dlo_stats(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int64), ("dp_size", ctypes.c_int64), ("slot_bytes", ctypes.c_int64),
+                ("device_weight_bytes", ctypes.c_int64), ("device_weight_high_water", ctypes.c_int64),
+                ("max_block_bytes", ctypes.c_int64), ("host_shard_bytes", ctypes.c_int64),
+                ("activation_bytes", ctypes.c_int64), ("forwards", ctypes.c_int64),
+                ("kernel_launches", ctypes.c_int64), ("fills", ctypes.c_int64), ("fill_mode", ctypes.c_int32),
+                ("resident", ctypes.c_int32), ("h2d_memcpy_gbs", ctypes.c_double),
+                ("h2d_zerocopy_gbs", ctypes.c_double)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+_c_i32, _c_i64, _c_u32, _c_p = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p
+_SIGS = {
+    "dlo_validate_spec": [ctypes.POINTER(dlo_block_spec)],
+    "dlo_block_numel": [ctypes.POINTER(dlo_block_spec), ctypes.POINTER(_c_i64)],
+    "dlo_shard_numel": [_c_i64, _c_i32, ctypes.POINTER(_c_i64)],
+    "dlo_param_table": [ctypes.POINTER(dlo_block_spec), ctypes.POINTER(_c_i64), ctypes.POINTER(_c_i64)],
+    "dlo_pack_block": [ctypes.POINTER(dlo_block_spec), ctypes.POINTER(_c_p), _c_i32, ctypes.POINTER(_c_p)],
+    "dlo_create": [ctypes.POINTER(dlo_block_spec), _c_i32, _c_i32, ctypes.POINTER(_c_p), _c_u32, ctypes.POINTER(_c_p)],
+    "dlo_forward": [_c_p, _c_p, _c_p, _c_i32, _c_i32, _c_p],
+    "dlo_forward_host": [_c_p, _c_p, _c_p, _c_i32, _c_i32, _c_p],
+    "dlo_synchronize": [_c_p, _c_i32],
+    "dlo_get_stats": [_c_p, ctypes.POINTER(dlo_stats)],
+    "dlo_get_kernel_times": [_c_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_c_i64)],
+    "dlo_debug_fill_and_read": [_c_p, _c_i32, _c_i32, _c_p, _c_i64],
+    "dlo_destroy": [_c_p],
+    "dlo_op_adaln": [_c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_p, _c_p],
+    "dlo_op_ln_modulate": [_c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p],
+    "dlo_op_linear": [_c_i32, _c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i32, _c_i32, _c_p],
+    "dlo_op_attention": [_c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p],
+    "dlo_op_shard_gather": [ctypes.POINTER(_c_p), _c_i32, _c_i64, _c_p, _c_p],
+    "dlo_op_check": [_c_p],
+}
+
+
+def lib():
+    """The loaded CUDA library; raises DloLibraryMissing if it is not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise DloLibraryMissing(
+                    f"{LIB_PATH} is missing: build it with `python -m layerwise_weight_offloaded_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, args in _SIGS.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            L.dlo_last_error.restype = ctypes.c_char_p
+            L.dlo_last_error.argtypes = []
+            L.dlo_status_string.restype = ctypes.c_char_p
+            L.dlo_status_string.argtypes = [ctypes.c_int]
+            _lib = L
+    return _lib
+
+
+def status_name(status: int) -> str:
+    try:
+        return lib().dlo_status_string(status).decode()
+    except DloLibraryMissing:
+        return f"status {status}"
+
+
+def _check(status: int):
+    if status != DLO_OK:
+        raise DloError(status, lib().dlo_last_error().decode())
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    if isinstance(x, ctypes.c_void_p):
+        return x.value
+    raise TypeError(f"cannot take a pointer of {type(x)}")
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s or None
+    return s.cuda_stream or None
+
+
+def _spec(s) -> dlo_block_spec:
+    if isinstance(s, dlo_block_spec):
+        return s
+    if isinstance(s, dict):
+        return dlo_block_spec(s["hidden"], s["num_heads"], s["mlp_hidden"], s["cond_dim"])
+    return dlo_block_spec(*s)
+
+
+# ---------------------------------------------------------------- host helpers
+def dlo_validate_spec(spec) -> None:
+    sp = _spec(spec)
+    _check(lib().dlo_validate_spec(ctypes.byref(sp)))
+
+
+def dlo_block_numel(spec) -> int:
+    sp, n = _spec(spec), _c_i64()
+    _check(lib().dlo_block_numel(ctypes.byref(sp), ctypes.byref(n)))
+    return n.value
+
+
+def dlo_shard_numel(numel: int, dp_size: int) -> int:
+    n = _c_i64()
+    _check(lib().dlo_shard_numel(numel, dp_size, ctypes.byref(n)))
+    return n.value
+
+
+def dlo_param_table(spec) -> tuple[list[int], list[int]]:
+    sp = _spec(spec)
+    offs, nums = (_c_i64 * DLO_NUM_PARAMS)(), (_c_i64 * DLO_NUM_PARAMS)()
+    _check(lib().dlo_param_table(ctypes.byref(sp), offs, nums))
+    return list(offs), list(nums)
+
+
+def dlo_pack_block(spec, params, dp_size: int, shards) -> None:
+    sp = _spec(spec)
+    pp = (_c_p * DLO_NUM_PARAMS)(*[_ptr(p) for p in params])
+    ss = (_c_p * dp_size)(*[_ptr(s) for s in shards])
+    _check(lib().dlo_pack_block(ctypes.byref(sp), pp, dp_size, ss))
+
+
+def dlo_last_error() -> str:
+    return lib().dlo_last_error().decode()
+
+
+def dlo_status_string(status: int) -> str:
+    return lib().dlo_status_string(status).decode()
+
+
+# ---------------------------------------------------------------- runtime
+def dlo_create(specs, dp_size: int, shard_ptrs, flags: int = DLO_FILL_AUTO) -> int:
+    """Returns the handle (an int); shard_ptrs[b * dp_size + r] = shard r of block b."""
+    arr = (dlo_block_spec * len(specs))(*[_spec(s) for s in specs])
+    ptrs = (_c_p * len(shard_ptrs))(*[_ptr(p) for p in shard_ptrs])
+    out = _c_p()
+    _check(lib().dlo_create(arr, len(specs), dp_size, ptrs, flags, ctypes.byref(out)))
+    return out.value
+
+
+def dlo_forward(handle: int, x, cond, num_requests: int, tokens_per_request: int, stream=None) -> None:
+    _check(lib().dlo_forward(handle, _ptr(x), _ptr(cond), num_requests, tokens_per_request, _stream(stream)))
+
+
+def dlo_forward_host(handle: int, x_host, cond_host, num_requests: int, tokens_per_request: int,
+                     stream=None) -> None:
+    _check(lib().dlo_forward_host(handle, _ptr(x_host), _ptr(cond_host), num_requests, tokens_per_request,
+                                  _stream(stream)))
+
+
+def dlo_synchronize(handle: int, timeout_ms: int = -1) -> None:
+    _check(lib().dlo_synchronize(handle, timeout_ms))
+
+
+def dlo_get_stats(handle: int) -> dict:
+    st = dlo_stats()
+    _check(lib().dlo_get_stats(handle, ctypes.byref(st)))
+    return {name: getattr(st, name) for name, _ in dlo_stats._fields_}
+
+
+def dlo_get_kernel_times(handle: int) -> dict:
+    ms, n = (ctypes.c_double * DLO_K_NUM)(), (_c_i64 * DLO_K_NUM)()
+    _check(lib().dlo_get_kernel_times(handle, ms, n))
+    return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_CLASSES)}
+
+
+def dlo_debug_fill_and_read(handle: int, block: int, slot: int, dst, nbytes: int) -> None:
+    _check(lib().dlo_debug_fill_and_read(handle, block, slot, _ptr(dst), nbytes))
+
+
+def dlo_destroy(handle: int) -> None:
+    if handle:
+        _check(lib().dlo_destroy(handle))
+
+
+# ---------------------------------------------------------------- single ops
+def dlo_op_adaln(ada_w, ada_b, cond, R: int, C: int, N: int, mod, stream=None) -> None:
+    _check(lib().dlo_op_adaln(_ptr(ada_w), _ptr(ada_b), _ptr(cond), R, C, N, _ptr(mod), _stream(stream)))
+
+
+def dlo_op_ln_modulate(x, shift, scale, mod_stride: int, R: int, T: int, hidden: int, u, stream=None) -> None:
+    _check(lib().dlo_op_ln_modulate(_ptr(x), _ptr(shift), _ptr(scale), mod_stride, R, T, hidden, _ptr(u),
+                                    _stream(stream)))
+
+
+def dlo_op_linear(epilogue: int, A, W, bias, M: int, N: int, K: int, out, gate=None, gate_stride: int = 0,
+                  T: int = 1, stream=None) -> None:
+    _check(lib().dlo_op_linear(epilogue, _ptr(A), _ptr(W), _ptr(bias), M, N, K, _ptr(out), _ptr(gate),
+                               gate_stride, T, _stream(stream)))
+
+
+def dlo_op_attention(qkv, R: int, T: int, H: int, d: int, o, stream=None) -> None:
+    _check(lib().dlo_op_attention(_ptr(qkv), R, T, H, d, _ptr(o), _stream(stream)))
+
+
+def dlo_op_shard_gather(shards, dp: int, S: int, dst, stream=None) -> None:
+    arr = (_c_p * dp)(*[_ptr(s) for s in shards])
+    _check(lib().dlo_op_shard_gather(arr, dp, S, _ptr(dst), _stream(stream)))
+
+
+def dlo_op_check(stream=None) -> None:
+    _check(lib().dlo_op_check(_stream(stream)))
+
+
+__all__ = [n for n in dir() if n.startswith(("dlo_", "DLO_"))] + [
+    "DloError", "DloLibraryMissing", "lib", "LIB_PATH", "PARAM_NAMES", "KERNEL_CLASSES", "EXPORTED", "status_name"]

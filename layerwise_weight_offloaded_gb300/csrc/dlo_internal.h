@@ -1,0 +1,70 @@
+// Internal declarations shared by the runtime and the kernel translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/dlo.h"
+
+namespace dlo {
+
+// Records a one-line message for dlo_last_error() and returns `status`.
+int set_error(int status, const char* fmt, ...);
+// Maps a CUDA runtime error to DLO_ERR_OOM / DLO_ERR_CUDA with a message.
+int cuda_error(cudaError_t e, const char* what);
+
+#define DLO_CUDA_TRY(expr)                                     \
+    do {                                                       \
+        cudaError_t _e = (expr);                               \
+        if (_e != cudaSuccess) return ::dlo::cuda_error(_e, #expr); \
+    } while (0)
+
+// Device properties the launchers need (cached per device).
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    size_t smem_optin = 0;
+};
+int device_info(DeviceInfo* out);
+
+// 2-D bf16 tensor map over a row-major [rows, inner] matrix with a
+// box of [box_rows, 64] elements and 128-byte swizzle.
+int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+
+// Process-wide device error word for the single-op entry points.
+int op_error_flag(int** flag);
+
+// ---------------------------------------------------------------- launchers
+// All return DLO_OK or an error status; all are asynchronous on `st`.
+
+int launch_shard_gather(const uint16_t* const* shards, int dp, int64_t S, uint16_t* dst, cudaStream_t st,
+                        int num_sms);
+
+int launch_adaln(const uint16_t* ada_w, const uint16_t* ada_b, const float* cond, int R, int C, int N,
+                 float* mod, cudaStream_t st);
+
+int launch_ln_modulate(const float* x, const float* shift, const float* scale, int mod_stride, int R, int T,
+                       int hidden, uint16_t* u, cudaStream_t st);
+
+struct GemmArgs {
+    int epilogue;  // DLO_EPI_*
+    int M, N, K;
+    const uint16_t* bias;
+    void* out;
+    const float* gate;
+    int gate_stride;
+    int T;
+    int* err;
+};
+// Tensor maps from encode_tmap_bf16: A over [M, K] with box rows 128; tmW[0]
+// and tmW[1] over W [N, K] with box rows 128 and 256 (the kernel picks its
+// tile width per shape).
+int gemm_block_n(int M, int N, int num_sms);
+int launch_gemm(const CUtensorMap& tmA, const CUtensorMap* tmW, const GemmArgs& a, cudaStream_t st, int num_sms);
+
+int launch_attention(const uint16_t* qkv, int R, int T, int H, int d, uint16_t* o, cudaStream_t st);
+
+}  // namespace dlo

@@ -1,0 +1,751 @@
+// Streaming runtime of the layerwise weight-offloaded DiT forward.
+//
+// "vLLM-Omni 发布 Distributed Layerwise Offload…", section 3 "double-buffered
+// prefetch with H2D + AllGather overlap" and its three-stream timeline figure:
+// exactly two device slots sized to the largest block; while the compute
+// stream runs block N from slot N%2, a copy stream rebuilds block N+1 in slot
+// (N+1)%2 from its dp_size host shards; compute waits on a "filled" event
+// before it starts a block, and the copy stream waits on the "freed" event of
+// block N-1 before it overwrites that block's slot.  Weight HBM is therefore
+// 2 x max_block_size whatever the depth.  On one GPU the section-2 all-gather
+// is the reassembly of the shards into the slot: either dp_size copy-engine
+// copies or the zero-copy gather kernel, whichever measured faster.
+#include <algorithm>
+#include <array>
+#include <chrono>
+#include <cstring>
+#include <mutex>
+#include <thread>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "dlo_internal.h"
+
+namespace dlo {
+
+int cuda_error(cudaError_t e, const char* what) {
+    const int st = (e == cudaErrorMemoryAllocation) ? DLO_ERR_OOM : DLO_ERR_CUDA;
+    set_error(st, "%s failed: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+    return st;
+}
+
+int device_info(DeviceInfo* out) {
+    static DeviceInfo cache[64];
+    static std::mutex mu;
+    int dev = 0;
+    DLO_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return set_error(DLO_ERR_INVALID_ARG, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev].device != dev) {
+        cudaDeviceProp p;
+        DLO_CUDA_TRY(cudaGetDeviceProperties(&p, dev));
+        DeviceInfo d;
+        d.device = dev;
+        d.num_sms = p.multiProcessorCount;
+        d.cc_major = p.major;
+        d.cc_minor = p.minor;
+        d.smem_optin = p.sharedMemPerBlockOptin;
+        cache[dev] = d;
+    }
+    *out = cache[dev];
+    if (out->cc_major != 10 || out->cc_minor != 3)
+        return set_error(DLO_ERR_UNSUPPORTED, "device is sm_%d%d; this library is built for sm_103a (GB300)",
+                         out->cc_major, out->cc_minor);
+    return DLO_OK;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    auto enc = tmap_encoder();
+    if (!enc) return set_error(DLO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    if (reinterpret_cast<uintptr_t>(base) % 16 || (inner * 2) % 16)
+        return set_error(DLO_ERR_ALIGNMENT, "tensor map: base or row pitch not 16-byte aligned");
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(DLO_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return DLO_OK;
+}
+
+int op_error_flag(int** flag) {
+    static int* flags[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    DLO_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return set_error(DLO_ERR_INVALID_ARG, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (!flags[dev]) {
+        int* p = nullptr;
+        DLO_CUDA_TRY(cudaMalloc(&p, sizeof(int)));
+        DLO_CUDA_TRY(cudaMemset(p, 0, sizeof(int)));
+        flags[dev] = p;
+    }
+    *flag = flags[dev];
+    return DLO_OK;
+}
+
+}  // namespace dlo
+
+using namespace dlo;
+
+// Weight tensor maps of one block in the slot it runs from (box 128 and 256 rows).
+struct BlockMaps {
+    CUtensorMap qkv[2], proj[2], fc1[2], fc2[2];
+};
+struct ActMaps {
+    CUtensorMap u, o, g;
+};
+
+struct ProfEvent {
+    int cls;
+    cudaEvent_t a, b;
+};
+
+struct dlo_handle {
+    DeviceInfo dev;
+    int L = 0, dp = 0;
+    uint32_t flags = 0;
+    int fill_mode = DLO_FILL_MEMCPY;
+    bool resident = false;
+    bool profile = false;
+    int status = DLO_OK;  // sticky error
+
+    std::vector<dlo_block_spec> specs;
+    std::vector<int64_t> numel, S;
+    std::vector<std::array<int64_t, DLO_NUM_PARAMS>> off;
+    std::vector<const uint16_t*> shard_host;  // [L*dp]
+    std::vector<const uint16_t*> shard_dev;   // device aliases of the mapped shards
+    std::vector<char> contiguous;             // shards of block b back to back in host memory
+    bool mapped = false;
+
+    int hidden = 0, cond_dim = 0, max_mlp = 0;
+    int64_t slot_elems = 0;
+    uint16_t* slot[2] = {nullptr, nullptr};
+    uint16_t* res_buf = nullptr;
+    std::vector<int64_t> res_off;
+    std::vector<BlockMaps> maps;
+
+    cudaStream_t copy = nullptr;
+    cudaEvent_t filled[2] = {}, freed[2] = {}, start_ev = nullptr, done_ev = nullptr;
+    int* d_err = nullptr;
+    bool work_pending = false;
+
+    // activations
+    int64_t rows_cap = 0, req_cap = 0;
+    float* mod = nullptr;
+    uint16_t *u = nullptr, *qkv = nullptr, *o = nullptr, *g = nullptr;
+    int64_t act_rows = -1;  // rows the activation maps were encoded for
+    std::vector<ActMaps> amaps;
+    // host-buffer forward staging
+    float* x_dev = nullptr;
+    float* c_dev = nullptr;
+    int64_t x_cap = 0, c_cap = 0;
+
+    std::vector<ProfEvent> prof_pool;
+    size_t prof_used = 0;
+
+    dlo_stats st{};
+};
+
+namespace {
+
+int fail(dlo_handle* h, int status) {
+    if (h && status != DLO_OK) h->status = status;
+    return status;
+}
+
+void add_weight_bytes(dlo_handle* h, int64_t b) {
+    h->st.device_weight_bytes += b;
+    h->st.device_weight_high_water = std::max(h->st.device_weight_high_water, h->st.device_weight_bytes);
+}
+
+// Issues the rebuild of block b into `dst` on the copy stream.
+int issue_fill(dlo_handle* h, int b, uint16_t* dst, int mode) {
+    const int64_t S = h->S[b];
+    const int64_t bytes = S * 2;
+    if (mode == DLO_FILL_ZEROCOPY) {
+        int rc = launch_shard_gather(&h->shard_dev[(size_t)b * h->dp], h->dp, S, dst, h->copy, h->dev.num_sms);
+        if (rc) return rc;
+        h->st.kernel_launches++;
+    } else if (h->contiguous[b]) {
+        DLO_CUDA_TRY(cudaMemcpyAsync(dst, h->shard_host[(size_t)b * h->dp], (size_t)bytes * h->dp,
+                                     cudaMemcpyHostToDevice, h->copy));
+    } else {
+        for (int r = 0; r < h->dp; ++r)
+            DLO_CUDA_TRY(cudaMemcpyAsync(dst + (size_t)r * S, h->shard_host[(size_t)b * h->dp + r], (size_t)bytes,
+                                         cudaMemcpyHostToDevice, h->copy));
+    }
+    h->st.fills++;
+    return DLO_OK;
+}
+
+ProfEvent* prof_begin(dlo_handle* h, int cls, cudaStream_t s) {
+    if (!h->profile) return nullptr;
+    if (h->prof_used == h->prof_pool.size()) {
+        ProfEvent e{cls, nullptr, nullptr};
+        if (cudaEventCreate(&e.a) != cudaSuccess || cudaEventCreate(&e.b) != cudaSuccess) return nullptr;
+        h->prof_pool.push_back(e);
+    }
+    ProfEvent* e = &h->prof_pool[h->prof_used++];
+    e->cls = cls;
+    cudaEventRecord(e->a, s);
+    return e;
+}
+void prof_end(ProfEvent* e, cudaStream_t s) {
+    if (e) cudaEventRecord(e->b, s);
+}
+
+int weights_base(dlo_handle* h, int b, const uint16_t** w) {
+    *w = h->resident ? h->res_buf + h->res_off[b] : h->slot[b & 1];
+    return DLO_OK;
+}
+
+int encode_block_maps(dlo_handle* h, int b) {
+    const uint16_t* w;
+    weights_base(h, b, &w);
+    const auto& sp = h->specs[b];
+    const auto& of = h->off[b];
+    const uint64_t hd = sp.hidden, m = sp.mlp_hidden;
+    BlockMaps& bm = h->maps[b];
+    for (int v = 0; v < 2; ++v) {
+        const uint32_t box = v ? 256 : 128;
+        int rc;
+        if ((rc = encode_tmap_bf16(&bm.qkv[v], w + of[DLO_P_QKV_W], hd, 3 * hd, box))) return rc;
+        if ((rc = encode_tmap_bf16(&bm.proj[v], w + of[DLO_P_PROJ_W], hd, hd, box))) return rc;
+        if ((rc = encode_tmap_bf16(&bm.fc1[v], w + of[DLO_P_FC1_W], hd, m, box))) return rc;
+        if ((rc = encode_tmap_bf16(&bm.fc2[v], w + of[DLO_P_FC2_W], m, hd, box))) return rc;
+    }
+    return DLO_OK;
+}
+
+template <typename T>
+int grow(T** p, int64_t* cap, int64_t need, int64_t* acct) {
+    if (need <= *cap) return DLO_OK;
+    if (*p) {
+        DLO_CUDA_TRY(cudaFree(*p));
+        if (acct) *acct -= *cap * (int64_t)sizeof(T);
+    }
+    *p = nullptr;
+    *cap = 0;
+    DLO_CUDA_TRY(cudaMalloc(p, (size_t)need * sizeof(T)));
+    *cap = need;
+    if (acct) *acct += need * (int64_t)sizeof(T);
+    return DLO_OK;
+}
+
+int ensure_activations(dlo_handle* h, int R, int T) {
+    const int64_t M = (int64_t)R * T;
+    if (M > h->rows_cap || R > h->req_cap) {
+        // (Re)allocate all scratch for max(M, cap) rows; the caller's stream order
+        // is respected because cudaFree/cudaMalloc synchronise the device.
+        const int64_t rows = std::max(M, h->rows_cap);
+        const int64_t reqs = std::max<int64_t>(R, h->req_cap);
+        int64_t dummy;
+        for (void** p : {(void**)&h->mod, (void**)&h->u, (void**)&h->qkv, (void**)&h->o, (void**)&h->g}) {
+            if (*p) DLO_CUDA_TRY(cudaFree(*p));
+            *p = nullptr;
+        }
+        h->st.activation_bytes = 0;
+        (void)dummy;
+        const int64_t hd = h->hidden;
+        DLO_CUDA_TRY(cudaMalloc(&h->mod, (size_t)reqs * 6 * hd * sizeof(float)));
+        DLO_CUDA_TRY(cudaMalloc(&h->u, (size_t)rows * hd * 2));
+        DLO_CUDA_TRY(cudaMalloc(&h->qkv, (size_t)rows * 3 * hd * 2));
+        DLO_CUDA_TRY(cudaMalloc(&h->o, (size_t)rows * hd * 2));
+        DLO_CUDA_TRY(cudaMalloc(&h->g, (size_t)rows * h->max_mlp * 2));
+        h->st.activation_bytes = reqs * 6 * hd * 4 + rows * hd * 2 * 5 + rows * (int64_t)h->max_mlp * 2;
+        h->rows_cap = rows;
+        h->req_cap = reqs;
+        h->act_rows = -1;
+    }
+    if (h->act_rows != M) {
+        for (int b = 0; b < h->L; ++b) {
+            const auto& sp = h->specs[b];
+            int rc;
+            if ((rc = encode_tmap_bf16(&h->amaps[b].u, h->u, sp.hidden, M, 128))) return rc;
+            if ((rc = encode_tmap_bf16(&h->amaps[b].o, h->o, sp.hidden, M, 128))) return rc;
+            if ((rc = encode_tmap_bf16(&h->amaps[b].g, h->g, sp.mlp_hidden, M, 128))) return rc;
+        }
+        h->act_rows = M;
+    }
+    return DLO_OK;
+}
+
+// The kernels of one block, all on the compute stream `s`.
+int run_block(dlo_handle* h, int b, float* x, const float* cond, int R, int T, cudaStream_t s) {
+    const auto& sp = h->specs[b];
+    const auto& of = h->off[b];
+    const int hd = sp.hidden, H = sp.num_heads, d = hd / H, m = sp.mlp_hidden, C = sp.cond_dim;
+    const int M = R * T;
+    const uint16_t* w;
+    weights_base(h, b, &w);
+    const BlockMaps& bm = h->maps[b];
+    const ActMaps& am = h->amaps[b];
+    float* mod = h->mod;
+    const int ms = 6 * hd;
+    int rc;
+    ProfEvent* e;
+
+    e = prof_begin(h, DLO_K_ADALN, s);
+    if ((rc = launch_adaln(w + of[DLO_P_ADA_W], w + of[DLO_P_ADA_B], cond, R, C, 6 * hd, mod, s))) return rc;
+    prof_end(e, s);
+
+    e = prof_begin(h, DLO_K_LN_MOD, s);
+    if ((rc = launch_ln_modulate(x, mod + 0 * hd, mod + 1 * hd, ms, R, T, hd, h->u, s))) return rc;
+    prof_end(e, s);
+
+    GemmArgs a{};
+    a.err = h->d_err;
+    a.M = M;
+    a.T = T;
+
+    e = prof_begin(h, DLO_K_GEMM_QKV, s);
+    a.epilogue = DLO_EPI_BIAS; a.N = 3 * hd; a.K = hd; a.bias = w + of[DLO_P_QKV_B]; a.out = h->qkv; a.gate = nullptr;
+    if ((rc = launch_gemm(am.u, bm.qkv, a, s, h->dev.num_sms))) return rc;
+    prof_end(e, s);
+
+    e = prof_begin(h, DLO_K_ATTENTION, s);
+    if ((rc = launch_attention(h->qkv, R, T, H, d, h->o, s))) return rc;
+    prof_end(e, s);
+
+    e = prof_begin(h, DLO_K_GEMM_PROJ, s);
+    a.epilogue = DLO_EPI_GATED_RESIDUAL; a.N = hd; a.K = hd; a.bias = w + of[DLO_P_PROJ_B]; a.out = x;
+    a.gate = mod + 2 * hd; a.gate_stride = ms;
+    if ((rc = launch_gemm(am.o, bm.proj, a, s, h->dev.num_sms))) return rc;
+    prof_end(e, s);
+
+    e = prof_begin(h, DLO_K_LN_MOD, s);
+    if ((rc = launch_ln_modulate(x, mod + 3 * hd, mod + 4 * hd, ms, R, T, hd, h->u, s))) return rc;
+    prof_end(e, s);
+
+    e = prof_begin(h, DLO_K_GEMM_FC1, s);
+    a.epilogue = DLO_EPI_BIAS_GELU; a.N = m; a.K = hd; a.bias = w + of[DLO_P_FC1_B]; a.out = h->g; a.gate = nullptr;
+    if ((rc = launch_gemm(am.u, bm.fc1, a, s, h->dev.num_sms))) return rc;
+    prof_end(e, s);
+
+    e = prof_begin(h, DLO_K_GEMM_FC2, s);
+    a.epilogue = DLO_EPI_GATED_RESIDUAL; a.N = hd; a.K = m; a.bias = w + of[DLO_P_FC2_B]; a.out = x;
+    a.gate = mod + 5 * hd; a.gate_stride = ms;
+    if ((rc = launch_gemm(am.g, bm.fc2, a, s, h->dev.num_sms))) return rc;
+    prof_end(e, s);
+
+    h->st.kernel_launches += 8;
+    return DLO_OK;
+}
+
+// Times `reps` fills of block 0 into slot 0 with `mode`; returns GB/s.
+double time_fill(dlo_handle* h, int mode, int reps) {
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) return 0;
+    if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); return 0; }
+    double gbs = 0;
+    if (issue_fill(h, 0, h->slot[0], mode) == DLO_OK && cudaEventRecord(a, h->copy) == cudaSuccess) {
+        bool ok = true;
+        for (int i = 0; i < reps && ok; ++i) ok = issue_fill(h, 0, h->slot[0], mode) == DLO_OK;
+        if (ok && cudaEventRecord(b, h->copy) == cudaSuccess && cudaEventSynchronize(b) == cudaSuccess) {
+            float ms = 0;
+            cudaEventElapsedTime(&ms, a, b);
+            if (ms > 0) gbs = (double)h->S[0] * 2 * h->dp * reps / (ms * 1e-3) / 1e9;
+        }
+    }
+    cudaEventDestroy(a);
+    cudaEventDestroy(b);
+    return gbs;
+}
+
+void release(dlo_handle* h) {
+    if (h->copy) cudaStreamSynchronize(h->copy);
+    if (h->done_ev) cudaEventSynchronize(h->done_ev);
+    for (auto* p : {(void*)h->slot[0], (void*)h->slot[1], (void*)h->res_buf, (void*)h->mod, (void*)h->u,
+                    (void*)h->qkv, (void*)h->o, (void*)h->g, (void*)h->x_dev, (void*)h->c_dev, (void*)h->d_err})
+        if (p) cudaFree(p);
+    for (int i = 0; i < 2; ++i) {
+        if (h->filled[i]) cudaEventDestroy(h->filled[i]);
+        if (h->freed[i]) cudaEventDestroy(h->freed[i]);
+    }
+    if (h->start_ev) cudaEventDestroy(h->start_ev);
+    if (h->done_ev) cudaEventDestroy(h->done_ev);
+    for (auto& e : h->prof_pool) {
+        cudaEventDestroy(e.a);
+        cudaEventDestroy(e.b);
+    }
+    if (h->copy) cudaStreamDestroy(h->copy);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dlo_create(const dlo_block_spec* specs, int32_t num_blocks, int32_t dp_size, const void* const* shard_ptrs,
+               uint32_t flags, dlo_handle** out) {
+    if (!out) return set_error(DLO_ERR_INVALID_ARG, "create: out is null");
+    *out = nullptr;
+    if (!specs || !shard_ptrs) return set_error(DLO_ERR_INVALID_ARG, "create: null specs or shard pointers");
+    if (num_blocks < 1) return set_error(DLO_ERR_INVALID_ARG, "create: num_blocks must be >= 1");
+    if (dp_size < 1 || dp_size > 64) return set_error(DLO_ERR_INVALID_ARG, "create: dp_size must be in [1, 64]");
+    if (flags & ~(uint32_t)(DLO_FILL_MASK | DLO_RESIDENT | DLO_PROFILE))
+        return set_error(DLO_ERR_INVALID_ARG, "create: unknown flag bits 0x%x", flags);
+    if ((flags & DLO_FILL_MASK) == DLO_FILL_MASK) return set_error(DLO_ERR_INVALID_ARG, "create: bad fill mode");
+
+    auto* h = new (std::nothrow) dlo_handle();
+    if (!h) return set_error(DLO_ERR_OOM, "create: host allocation failed");
+    int rc = device_info(&h->dev);
+    if (rc) { delete h; return rc; }
+    h->L = num_blocks;
+    h->dp = dp_size;
+    h->flags = flags;
+    h->resident = (flags & DLO_RESIDENT) != 0;
+    h->profile = (flags & DLO_PROFILE) != 0;
+    h->specs.assign(specs, specs + num_blocks);
+    h->numel.resize(num_blocks);
+    h->S.resize(num_blocks);
+    h->off.resize(num_blocks);
+    h->contiguous.assign(num_blocks, 0);
+    h->maps.resize(num_blocks);
+    h->amaps.resize(num_blocks);
+    h->hidden = specs[0].hidden;
+    h->cond_dim = specs[0].cond_dim;
+    auto bail = [&](int status) {
+        release(h);
+        delete h;
+        return status;
+    };
+    for (int b = 0; b < num_blocks; ++b) {
+        if ((rc = dlo_validate_spec(&specs[b]))) return bail(rc);
+        if (specs[b].hidden != h->hidden || specs[b].cond_dim != h->cond_dim)
+            return bail(set_error(DLO_ERR_SHAPE, "create: block %d hidden/cond_dim differ from block 0", b));
+        int64_t n[DLO_NUM_PARAMS];
+        dlo_param_table(&specs[b], h->off[b].data(), n);
+        dlo_block_numel(&specs[b], &h->numel[b]);
+        dlo_shard_numel(h->numel[b], dp_size, &h->S[b]);
+        h->slot_elems = std::max(h->slot_elems, h->S[b] * dp_size);
+        h->max_mlp = std::max(h->max_mlp, specs[b].mlp_hidden);
+        h->st.max_block_bytes = std::max<int64_t>(h->st.max_block_bytes, h->numel[b] * 2);
+        h->st.host_shard_bytes += h->S[b] * dp_size * 2;
+    }
+    const size_t nsh = (size_t)num_blocks * dp_size;
+    h->shard_host.resize(nsh);
+    h->shard_dev.resize(nsh);
+    bool mapped = true;
+    for (size_t i = 0; i < nsh; ++i) {
+        if (!shard_ptrs[i]) return bail(set_error(DLO_ERR_INVALID_ARG, "create: shard pointer %zu is null", i));
+        h->shard_host[i] = static_cast<const uint16_t*>(shard_ptrs[i]);
+        cudaPointerAttributes attr{};
+        if (cudaPointerGetAttributes(&attr, shard_ptrs[i]) == cudaSuccess && attr.type == cudaMemoryTypeHost &&
+            attr.devicePointer)
+            h->shard_dev[i] = static_cast<const uint16_t*>(attr.devicePointer);
+        else
+            mapped = false;
+        cudaGetLastError();  // clear a sticky "invalid value" from unregistered pointers
+    }
+    h->mapped = mapped;
+    for (int b = 0; b < num_blocks; ++b) {
+        bool c = true;
+        for (int r = 1; r < dp_size; ++r)
+            c = c && h->shard_host[(size_t)b * dp_size + r] == h->shard_host[(size_t)b * dp_size] + (size_t)r * h->S[b];
+        h->contiguous[b] = c;
+    }
+    int mode = flags & DLO_FILL_MASK;
+    if (mode == DLO_FILL_ZEROCOPY && !mapped)
+        return bail(set_error(DLO_ERR_INVALID_ARG, "create: zero-copy fill needs mapped page-locked shards"));
+
+    cudaError_t e;
+    if ((e = cudaStreamCreateWithFlags(&h->copy, cudaStreamNonBlocking)) != cudaSuccess)
+        return bail(cuda_error(e, "cudaStreamCreate"));
+    for (int i = 0; i < 2; ++i) {
+        if ((e = cudaEventCreateWithFlags(&h->filled[i], cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&h->freed[i], cudaEventDisableTiming)) != cudaSuccess)
+            return bail(cuda_error(e, "cudaEventCreate"));
+    }
+    if ((e = cudaEventCreateWithFlags(&h->start_ev, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&h->done_ev, cudaEventDisableTiming)) != cudaSuccess)
+        return bail(cuda_error(e, "cudaEventCreate"));
+    if ((e = cudaMalloc(&h->d_err, sizeof(int))) != cudaSuccess) return bail(cuda_error(e, "cudaMalloc(err)"));
+    if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess) return bail(cuda_error(e, "cudaMemset"));
+
+    // The two slots (also used by the fill timing and debug access in resident mode).
+    h->st.slot_bytes = h->slot_elems * 2;
+    for (int s = 0; s < 2; ++s) {
+        if ((e = cudaMalloc(&h->slot[s], (size_t)h->st.slot_bytes)) != cudaSuccess)
+            return bail(cuda_error(e, "cudaMalloc(slot)"));
+        add_weight_bytes(h, h->st.slot_bytes);
+    }
+    if (mode == DLO_FILL_AUTO) {
+        mode = DLO_FILL_MEMCPY;
+        h->st.h2d_memcpy_gbs = time_fill(h, DLO_FILL_MEMCPY, 3);
+        if (mapped) {
+            h->st.h2d_zerocopy_gbs = time_fill(h, DLO_FILL_ZEROCOPY, 3);
+            if (h->st.h2d_zerocopy_gbs > h->st.h2d_memcpy_gbs) mode = DLO_FILL_ZEROCOPY;
+        }
+        if ((e = cudaStreamSynchronize(h->copy)) != cudaSuccess) return bail(cuda_error(e, "fill timing"));
+    }
+    h->fill_mode = mode;
+    h->st.fill_mode = mode;
+
+    if (h->resident) {
+        int64_t total = 0;
+        h->res_off.resize(num_blocks);
+        for (int b = 0; b < num_blocks; ++b) {
+            h->res_off[b] = total;
+            total += h->S[b] * dp_size;
+        }
+        if ((e = cudaMalloc(&h->res_buf, (size_t)total * 2)) != cudaSuccess)
+            return bail(cuda_error(e, "cudaMalloc(resident)"));
+        add_weight_bytes(h, total * 2);
+        for (int b = 0; b < num_blocks; ++b)
+            if ((rc = issue_fill(h, b, h->res_buf + h->res_off[b], mode))) return bail(rc);
+        if ((e = cudaStreamSynchronize(h->copy)) != cudaSuccess) return bail(cuda_error(e, "resident fill"));
+    }
+    for (int b = 0; b < num_blocks; ++b)
+        if ((rc = encode_block_maps(h, b))) return bail(rc);
+    h->st.num_blocks = num_blocks;
+    h->st.dp_size = dp_size;
+    h->st.resident = h->resident ? 1 : 0;
+    *out = h;
+    return DLO_OK;
+}
+
+int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T, dlo_stream_t stream) {
+    if (!h) return set_error(DLO_ERR_INVALID_ARG, "forward: null handle");
+    if (h->status) return set_error(DLO_ERR_STATE, "forward: handle is in an error state (%s)",
+                                    dlo_status_string(h->status));
+    if (!x || !cond) return set_error(DLO_ERR_INVALID_ARG, "forward: null x or cond");
+    if (R < 1 || T < 1) return set_error(DLO_ERR_INVALID_ARG, "forward: R and T must be >= 1");
+    if (R > 65535) return set_error(DLO_ERR_SHAPE, "forward: at most 65535 requests");
+    if ((int64_t)R * T > 0x7FFFFFFF) return set_error(DLO_ERR_SHAPE, "forward: R*T above 2^31-1");
+    if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(cond) % 4)
+        return set_error(DLO_ERR_ALIGNMENT, "forward: x must be 16-byte aligned, cond 4-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int rc;
+    if ((rc = ensure_activations(h, R, T))) return fail(h, rc);
+    h->prof_used = 0;
+    cudaError_t e;
+#define FWD_TRY(expr)                                            \
+    do {                                                         \
+        if ((e = (expr)) != cudaSuccess) return fail(h, cuda_error(e, #expr)); \
+    } while (0)
+    if (!h->resident) {
+        // Slots may still be read by earlier work on `s`: the first fill waits for it.
+        FWD_TRY(cudaEventRecord(h->start_ev, s));
+        FWD_TRY(cudaStreamWaitEvent(h->copy, h->start_ev, 0));
+        ProfEvent* pe = h->fill_mode == DLO_FILL_ZEROCOPY ? prof_begin(h, DLO_K_FILL, h->copy) : nullptr;
+        if ((rc = issue_fill(h, 0, h->slot[0], h->fill_mode))) return fail(h, rc);
+        prof_end(pe, h->copy);
+        FWD_TRY(cudaEventRecord(h->filled[0], h->copy));
+    }
+    for (int N = 0; N < h->L; ++N) {
+        const int slot = N & 1;
+        if (!h->resident) {
+            if (N + 1 < h->L) {
+                const int ns = (N + 1) & 1;
+                if (N + 1 >= 2) FWD_TRY(cudaStreamWaitEvent(h->copy, h->freed[ns], 0));
+                ProfEvent* pe = h->fill_mode == DLO_FILL_ZEROCOPY ? prof_begin(h, DLO_K_FILL, h->copy) : nullptr;
+                if ((rc = issue_fill(h, N + 1, h->slot[ns], h->fill_mode))) return fail(h, rc);
+                prof_end(pe, h->copy);
+                FWD_TRY(cudaEventRecord(h->filled[ns], h->copy));
+            }
+            FWD_TRY(cudaStreamWaitEvent(s, h->filled[slot], 0));
+        }
+        if ((rc = run_block(h, N, x, cond, R, T, s))) return fail(h, rc);
+        if (!h->resident) FWD_TRY(cudaEventRecord(h->freed[slot], s));
+    }
+    FWD_TRY(cudaEventRecord(h->done_ev, s));
+#undef FWD_TRY
+    h->work_pending = true;
+    h->st.forwards++;
+    return DLO_OK;
+}
+
+int dlo_forward_host(dlo_handle* h, float* x_host, const float* cond_host, int32_t R, int32_t T,
+                     dlo_stream_t stream) {
+    if (!h) return set_error(DLO_ERR_INVALID_ARG, "forward_host: null handle");
+    if (h->status) return set_error(DLO_ERR_STATE, "forward_host: handle is in an error state");
+    if (!x_host || !cond_host) return set_error(DLO_ERR_INVALID_ARG, "forward_host: null buffer");
+    if (R < 1 || T < 1) return set_error(DLO_ERR_INVALID_ARG, "forward_host: R and T must be >= 1");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t nx = (int64_t)R * T * h->hidden, nc = (int64_t)R * h->cond_dim;
+    int rc;
+    if ((rc = grow(&h->x_dev, &h->x_cap, nx, nullptr))) return fail(h, rc);
+    if ((rc = grow(&h->c_dev, &h->c_cap, nc, nullptr))) return fail(h, rc);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(h->x_dev, x_host, (size_t)nx * 4, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(h->c_dev, cond_host, (size_t)nc * 4, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+        return fail(h, cuda_error(e, "forward_host: H2D"));
+    if ((rc = dlo_forward(h, h->x_dev, h->c_dev, R, T, stream))) return rc;
+    if ((e = cudaMemcpyAsync(x_host, h->x_dev, (size_t)nx * 4, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+        return fail(h, cuda_error(e, "forward_host: D2H"));
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail(h, cuda_error(e, "forward_host: sync"));
+    int flag = 0;
+    if ((e = cudaMemcpy(&flag, h->d_err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return fail(h, cuda_error(e, "forward_host: error word"));
+    if (flag) return fail(h, set_error(DLO_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (code 0x%x)", flag));
+    return DLO_OK;
+}
+
+int dlo_synchronize(dlo_handle* h, int32_t timeout_ms) {
+    if (!h) return set_error(DLO_ERR_INVALID_ARG, "synchronize: null handle");
+    if (h->status) return set_error(DLO_ERR_STATE, "synchronize: handle is in an error state");
+    const auto t0 = std::chrono::steady_clock::now();
+    for (cudaStream_t q : {(cudaStream_t)nullptr, h->copy}) {
+        for (;;) {
+            cudaError_t e = q ? cudaStreamQuery(q) : (h->work_pending ? cudaEventQuery(h->done_ev) : cudaSuccess);
+            if (e == cudaSuccess) break;
+            if (e != cudaErrorNotReady) return fail(h, cuda_error(e, "synchronize"));
+            const auto ms =
+                std::chrono::duration_cast<std::chrono::milliseconds>(std::chrono::steady_clock::now() - t0).count();
+            if (timeout_ms >= 0 && ms >= timeout_ms)
+                return fail(h, set_error(DLO_ERR_TIMEOUT, "synchronize: work still running after %d ms", timeout_ms));
+            std::this_thread::sleep_for(std::chrono::microseconds(100));
+        }
+    }
+    h->work_pending = false;
+    int flag = 0;
+    cudaError_t e = cudaMemcpy(&flag, h->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail(h, cuda_error(e, "synchronize: error word"));
+    if (flag) return fail(h, set_error(DLO_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (code 0x%x)", flag));
+    return DLO_OK;
+}
+
+int dlo_get_stats(dlo_handle* h, dlo_stats* out) {
+    if (!h || !out) return set_error(DLO_ERR_INVALID_ARG, "get_stats: null pointer");
+    *out = h->st;
+    return DLO_OK;
+}
+
+int dlo_get_kernel_times(dlo_handle* h, double* ms, int64_t* launches) {
+    if (!h || !ms || !launches) return set_error(DLO_ERR_INVALID_ARG, "get_kernel_times: null pointer");
+    if (!h->profile) return set_error(DLO_ERR_STATE, "get_kernel_times: handle created without DLO_PROFILE");
+    for (int k = 0; k < DLO_K_NUM; ++k) {
+        ms[k] = 0;
+        launches[k] = 0;
+    }
+    for (size_t i = 0; i < h->prof_used; ++i) {
+        const ProfEvent& e = h->prof_pool[i];
+        cudaError_t err = cudaEventSynchronize(e.b);
+        if (err != cudaSuccess) return fail(h, cuda_error(err, "get_kernel_times"));
+        float t = 0;
+        if ((err = cudaEventElapsedTime(&t, e.a, e.b)) != cudaSuccess) return fail(h, cuda_error(err, "elapsed"));
+        ms[e.cls] += t;
+        launches[e.cls] += 1;
+    }
+    return DLO_OK;
+}
+
+int dlo_debug_fill_and_read(dlo_handle* h, int32_t block, int32_t slot, void* dst, int64_t bytes) {
+    if (!h || !dst) return set_error(DLO_ERR_INVALID_ARG, "debug_fill: null pointer");
+    if (h->status) return set_error(DLO_ERR_STATE, "debug_fill: handle is in an error state");
+    if (block < 0 || block >= h->L || slot < 0 || slot > 1 || bytes < 0 || bytes > h->st.slot_bytes)
+        return set_error(DLO_ERR_INVALID_ARG, "debug_fill: block, slot or size out of range");
+    int rc;
+    cudaError_t e;
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail(h, cuda_error(e, "debug_fill: sync"));
+    if ((rc = issue_fill(h, block, h->slot[slot], h->fill_mode))) return fail(h, rc);
+    if ((e = cudaStreamSynchronize(h->copy)) != cudaSuccess) return fail(h, cuda_error(e, "debug_fill: fill"));
+    if ((e = cudaMemcpy(dst, h->slot[slot], (size_t)bytes, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return fail(h, cuda_error(e, "debug_fill: read"));
+    // A resident handle's forward does not read the slots; a streamed one
+    // refills them at the start of every forward, so nothing else is disturbed.
+    return DLO_OK;
+}
+
+int dlo_destroy(dlo_handle* h) {
+    if (!h) return DLO_OK;
+    release(h);
+    delete h;
+    return DLO_OK;
+}
+
+// ------------------------------------------------------------ single-op entry points
+
+int dlo_op_adaln(const uint16_t* ada_w, const uint16_t* ada_b, const float* cond, int32_t R, int32_t C, int32_t N,
+                 float* mod, dlo_stream_t stream) {
+    DeviceInfo d;
+    int rc = device_info(&d);
+    if (rc) return rc;
+    return launch_adaln(ada_w, ada_b, cond, R, C, N, mod, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dlo_op_ln_modulate(const float* x, const float* shift, const float* scale, int32_t mod_stride, int32_t R,
+                       int32_t T, int32_t hidden, uint16_t* u, dlo_stream_t stream) {
+    DeviceInfo d;
+    int rc = device_info(&d);
+    if (rc) return rc;
+    if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(shift) % 16 ||
+        reinterpret_cast<uintptr_t>(scale) % 16 || reinterpret_cast<uintptr_t>(u) % 8)
+        return set_error(DLO_ERR_ALIGNMENT, "ln_modulate: x/shift/scale need 16-byte, u 8-byte alignment");
+    return launch_ln_modulate(x, shift, scale, mod_stride, R, T, hidden, u, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dlo_op_linear(int32_t epilogue, const uint16_t* A, const uint16_t* W, const uint16_t* bias, int32_t M, int32_t N,
+                  int32_t K, void* out, const float* gate, int32_t gate_stride, int32_t T, dlo_stream_t stream) {
+    DeviceInfo d;
+    int rc = device_info(&d);
+    if (rc) return rc;
+    if (!A || !W || !bias || !out) return set_error(DLO_ERR_INVALID_ARG, "linear: null pointer");
+    if (M <= 0 || N <= 0 || K <= 0) return set_error(DLO_ERR_INVALID_ARG, "linear: non-positive size");
+    if (N % 8 || K % 8) return set_error(DLO_ERR_ALIGNMENT, "linear: N and K must be multiples of 8");
+    if (reinterpret_cast<uintptr_t>(bias) % 16 || reinterpret_cast<uintptr_t>(out) % 16 ||
+        (gate && reinterpret_cast<uintptr_t>(gate) % 16))
+        return set_error(DLO_ERR_ALIGNMENT, "linear: bias, out and gate must be 16-byte aligned");
+    int* err = nullptr;
+    if ((rc = op_error_flag(&err))) return rc;
+    CUtensorMap ta, tw[2];
+    if ((rc = encode_tmap_bf16(&ta, A, (uint64_t)K, (uint64_t)M, 128))) return rc;
+    if ((rc = encode_tmap_bf16(&tw[0], W, (uint64_t)K, (uint64_t)N, 128))) return rc;
+    if ((rc = encode_tmap_bf16(&tw[1], W, (uint64_t)K, (uint64_t)N, 256))) return rc;
+    GemmArgs a{epilogue, M, N, K, bias, out, gate, gate_stride, T, err};
+    return launch_gemm(ta, tw, a, reinterpret_cast<cudaStream_t>(stream), d.num_sms);
+}
+
+int dlo_op_attention(const uint16_t* qkv, int32_t R, int32_t T, int32_t H, int32_t d, uint16_t* o,
+                     dlo_stream_t stream) {
+    DeviceInfo di;
+    int rc = device_info(&di);
+    if (rc) return rc;
+    if (reinterpret_cast<uintptr_t>(qkv) % 16 || reinterpret_cast<uintptr_t>(o) % 16)
+        return set_error(DLO_ERR_ALIGNMENT, "attention: qkv and o must be 16-byte aligned");
+    return launch_attention(qkv, R, T, H, d, o, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dlo_op_shard_gather(const uint16_t* const* shards, int32_t dp, int64_t S, uint16_t* dst, dlo_stream_t stream) {
+    DeviceInfo di;
+    int rc = device_info(&di);
+    if (rc) return rc;
+    return launch_shard_gather(shards, dp, S, dst, reinterpret_cast<cudaStream_t>(stream), di.num_sms);
+}
+
+int dlo_op_check(dlo_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_error(e, "op_check: sync");
+    int* err = nullptr;
+    int rc = op_error_flag(&err);
+    if (rc) return rc;
+    int flag = 0;
+    if ((e = cudaMemcpy(&flag, err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_error(e, "op_check: read flag");
+    if (flag) {
+        cudaMemset(err, 0, sizeof(int));
+        return set_error(DLO_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (code 0x%x)", flag);
+    }
+    return DLO_OK;
+}
+
+}  // extern "C"

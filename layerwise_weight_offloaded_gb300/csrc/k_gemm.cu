@@ -1,0 +1,301 @@
+// Linear layers of the DiT block on the 5th-generation tensor cores.
+//
+// out = epilogue(A . W^T + bias) with A bf16 [M, K] (activations) and W bf16
+// [N, K] read straight from the active weight slot ("vLLM-Omni 发布
+// Distributed Layerwise Offload…", section 3: parameters are views of the
+// rebuilt buffer).  Both operands are K-major, fp32 accumulation in TMEM.
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0     TMA producer: 128x64 A box and BNx64 W box per stage into a
+//              STAGES-deep shared-memory ring (128-byte swizzle);
+//   warp 1     allocates 2*BN TMEM columns; lane 0 issues tcgen05.mma
+//              (M=128, N=BN, K=16 per instruction) and commits each stage back
+//              to the producer and each finished tile to the epilogue;
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//              lanes 32*(w%4)..+31 = its 32 rows), bias + GELU or gated
+//              residual, global stores.  Two accumulators alternate, so the
+//              epilogue of tile i overlaps the MMAs of tile i+1.
+// Tiles are walked M-fastest so CTAs running together share a W panel in L2.
+// Every wait is bounded (dlo_device.cuh); on expiry the kernel records an
+// error code, waits for its own copies and MMAs, frees TMEM and returns.
+#include "dlo_device.cuh"
+#include "dlo_internal.h"
+
+namespace dlo {
+
+constexpr int kGemmBM = 128;
+constexpr int kGemmBK = 64;
+constexpr int kGemmThreads = 192;
+
+template <int BN>
+struct GemmCfg {
+    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static constexpr int kABytes = kGemmBM * kGemmBK * 2;
+    static constexpr int kBBytes = BN * kGemmBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kBarBytes = 256;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + kBarBytes;
+    static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
+};
+
+struct GemmDevArgs {
+    int M, N, K;
+    const uint16_t* bias;
+    void* out;
+    const float* gate;
+    int gate_stride;
+    int T;
+    int* err;
+};
+
+__device__ __forceinline__ float gelu_tanh_f(float v) {
+    const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+    return 0.5f * v * (1.0f + tanhf(k0 * (v + 0.044715f * v * v * v)));
+}
+
+// Epilogue of one row segment of 32 accumulator columns starting at col0.
+template <int EPI>
+__device__ __forceinline__ void epilogue_32(const GemmDevArgs& p, int row, int col0, const float* acc) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int col = col0 + 8 * g;
+        if (col >= p.N) break;
+        const uint4 bw = __ldg(reinterpret_cast<const uint4*>(p.bias + col));
+        float b[8] = {bf16_lo(bw.x), bf16_hi(bw.x), bf16_lo(bw.y), bf16_hi(bw.y),
+                      bf16_lo(bw.z), bf16_hi(bw.z), bf16_lo(bw.w), bf16_hi(bw.w)};
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = acc[8 * g + i] + b[i];
+        if constexpr (EPI == DLO_EPI_GATED_RESIDUAL) {
+            float* x = reinterpret_cast<float*>(p.out) + (size_t)row * p.N + col;
+            const float* gt = p.gate + (size_t)(row / p.T) * p.gate_stride + col;
+            const float4 g0 = *reinterpret_cast<const float4*>(gt);
+            const float4 g1 = *reinterpret_cast<const float4*>(gt + 4);
+            float4 x0 = *reinterpret_cast<float4*>(x);
+            float4 x1 = *reinterpret_cast<float4*>(x + 4);
+            x0.x += g0.x * v[0]; x0.y += g0.y * v[1]; x0.z += g0.z * v[2]; x0.w += g0.w * v[3];
+            x1.x += g1.x * v[4]; x1.y += g1.y * v[5]; x1.z += g1.z * v[6]; x1.w += g1.w * v[7];
+            *reinterpret_cast<float4*>(x) = x0;
+            *reinterpret_cast<float4*>(x + 4) = x1;
+        } else {
+            if constexpr (EPI == DLO_EPI_BIAS_GELU) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = gelu_tanh_f(v[i]);
+            }
+            uint4 o;
+            o.x = pack_bf16x2(v[0], v[1]);
+            o.y = pack_bf16x2(v[2], v[3]);
+            o.z = pack_bf16x2(v[4], v[5]);
+            o.w = pack_bf16x2(v[6], v[7]);
+            *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + (size_t)row * p.N + col) = o;
+        }
+    }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_bf16_tcgen05(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                      const GemmDevArgs p) {
+    using Cfg = GemmCfg<BN>;
+    constexpr int S = Cfg::kStages;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStageBytes);
+    uint64_t* empty = full + S;
+    uint64_t* acc_full = empty + S;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_m = (p.M + kGemmBM - 1) / kGemmBM;
+    const int num_n = (p.N + BN - 1) / BN;
+    const int num_tiles = num_m * num_n;
+    const int num_kb = (p.K + kGemmBK - 1) / kGemmBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 128);
+        }
+        mbar_init(drain, 1);
+        fence_mbarrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmW);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            long issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                const int m0 = (tile % num_m) * kGemmBM;
+                const int n0 = (tile / num_m) * BN;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.err, KERR_GEMM_PRODUCER)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * Cfg::kStageBytes;
+                    mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+                    tma_load_2d(sa, &tmA, kb * kGemmBK, m0, &full[stage]);
+                    tma_load_2d(sa + Cfg::kABytes, &tmW, kb * kGemmBK, n0, &full[stage]);
+                    ++issued;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Every copy this thread started must land before the CTA exits.
+            const long first = issued > S ? issued - S : 0;
+            for (long j = first; j < issued; ++j)
+                mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), p.err, KERR_GEMM_DRAIN);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = umma_idesc_bf16_f32(kGemmBM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, p.err, KERR_GEMM_MMA)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_bounded(&full[stage], phase, p.err, KERR_GEMM_MMA)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * Cfg::kStageBytes);
+                    const uint32_t b_addr = a_addr + Cfg::kABytes;
+#pragma unroll
+                    for (int k = 0; k < kGemmBK / 16; ++k) {
+                        umma_bf16(d_tmem, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32), idesc,
+                                  (kb | k) != 0);
+                    }
+                    umma_commit(&empty[stage]);  // stage is free once these MMAs have read it
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(&acc_full[acc]);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            // All MMAs issued here must finish before TMEM is released.
+            umma_commit(drain);
+            mbar_wait_bounded(drain, 0, p.err, KERR_GEMM_DRAIN);
+        }
+    } else {
+        // ---------------- epilogue warps 2..5
+        const int quarter = warp & 3;
+        const int row_in_tile = quarter * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const int m0 = (tile % num_m) * kGemmBM;
+            const int n0 = (tile / num_m) * BN;
+            if (!mbar_wait_bounded(&acc_full[acc], acc_phase, p.err, KERR_GEMM_EPILOGUE)) break;
+            tc_fence_after();
+            const int row = m0 + row_in_tile;
+            const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                float v[32];
+                tmem_ld_32x32b_x32(taddr + (uint32_t)c, v);
+                if (row < p.M && n0 + c < p.N) epilogue_32<EPI>(p, row, n0 + c, v);
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+int gemm_block_n(int M, int N, int num_sms) {
+    // Estimated time ~ waves x per-tile time; a 128-wide tile costs a bit more
+    // than half a 256-wide one (same A traffic, half the MMA work).
+    const long m_tiles = (M + kGemmBM - 1) / kGemmBM;
+    const long t256 = m_tiles * ((N + 255) / 256);
+    const long t128 = m_tiles * ((N + 127) / 128);
+    const double w256 = (double)((t256 + num_sms - 1) / num_sms);
+    const double w128 = (double)((t128 + num_sms - 1) / num_sms);
+    const double cost256 = w256 * 1.0;
+    const double cost128 = w128 * 0.56;
+    return cost128 < cost256 ? 128 : 256;
+}
+
+template <int BN, int EPI>
+static int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmW, const GemmDevArgs& d, cudaStream_t st,
+                         int num_sms) {
+    using Cfg = GemmCfg<BN>;
+    static bool configured[64] = {};
+    int dev = 0;
+    DLO_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return set_error(DLO_ERR_INVALID_ARG, "device index %d out of range", dev);
+    if (!configured[dev]) {
+        DLO_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_tcgen05<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          Cfg::kSmemBytes));
+        configured[dev] = true;
+    }
+    const int tiles = ((d.M + kGemmBM - 1) / kGemmBM) * ((d.N + BN - 1) / BN);
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    gemm_bf16_tcgen05<BN, EPI><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmA, tmW, d);
+    DLO_CUDA_TRY(cudaGetLastError());
+    return DLO_OK;
+}
+
+int launch_gemm(const CUtensorMap& tmA, const CUtensorMap* tmWs, const GemmArgs& a, cudaStream_t st, int num_sms) {
+    if (a.M <= 0 || a.N <= 0 || a.K <= 0) return set_error(DLO_ERR_INVALID_ARG, "gemm: non-positive size");
+    if (a.N % 8 || a.K % 8) return set_error(DLO_ERR_ALIGNMENT, "gemm: N and K must be multiples of 8");
+    if (!a.bias || !a.out || !a.err) return set_error(DLO_ERR_INVALID_ARG, "gemm: null pointer");
+    if (a.epilogue == DLO_EPI_GATED_RESIDUAL && (!a.gate || a.T <= 0 || a.gate_stride % 4))
+        return set_error(DLO_ERR_INVALID_ARG, "gemm: gated residual needs gate, T > 0, gate_stride % 4 == 0");
+    GemmDevArgs d{a.M, a.N, a.K, a.bias, a.out, a.gate, a.gate_stride, a.T, a.err};
+    const int bn = gemm_block_n(a.M, a.N, num_sms);
+    const CUtensorMap& tmW = tmWs[bn == 256 ? 1 : 0];
+    switch (a.epilogue * 2 + (bn == 256 ? 1 : 0)) {
+        case DLO_EPI_BIAS * 2: return launch_gemm_t<128, DLO_EPI_BIAS>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_BIAS * 2 + 1: return launch_gemm_t<256, DLO_EPI_BIAS>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_BIAS_GELU * 2: return launch_gemm_t<128, DLO_EPI_BIAS_GELU>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_BIAS_GELU * 2 + 1: return launch_gemm_t<256, DLO_EPI_BIAS_GELU>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_GATED_RESIDUAL * 2:
+            return launch_gemm_t<128, DLO_EPI_GATED_RESIDUAL>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_GATED_RESIDUAL * 2 + 1:
+            return launch_gemm_t<256, DLO_EPI_GATED_RESIDUAL>(tmA, tmW, d, st, num_sms);
+        default: return set_error(DLO_ERR_INVALID_ARG, "gemm: unknown epilogue %d", a.epilogue);
+    }
+}
+
+}  // namespace dlo

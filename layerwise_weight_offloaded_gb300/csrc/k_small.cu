@@ -1,0 +1,215 @@
+// The bandwidth-bound kernels of the streaming forward:
+//   * shard gather - the one-GPU stand-in for the all-gather of section 2 of
+//     "vLLM-Omni 发布 Distributed Layerwise Offload…": dst[r*S + i] = shard_r[i],
+//     read straight from mapped pinned host memory with 16-byte loads;
+//   * adaLN modulation GEMV - mod[R, 6h] = ada_w . SiLU(c) + ada_b;
+//   * LayerNorm + modulate - u = bf16(LN(x) * (1 + scale) + shift).
+#include "dlo_device.cuh"
+#include "dlo_internal.h"
+
+namespace dlo {
+
+// ------------------------------------------------------------------ shard gather
+
+constexpr int kMaxGatherShards = 64;
+struct ShardPtrs {
+    const uint16_t* p[kMaxGatherShards];
+};
+
+// Vector path: S % 8 == 0 and every pointer 16-byte aligned, so each 16-byte
+// destination chunk comes from one shard.  Each thread keeps 4 loads in flight.
+__global__ void __launch_bounds__(512) shard_gather_vec(ShardPtrs src, int dp, int64_t S, uint16_t* __restrict__ dst) {
+    const int64_t chunks_per_shard = S / 8;
+    const int64_t total = chunks_per_shard * dp;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < total; i += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t c = i + u * stride;
+            const int r = (int)(c / chunks_per_shard);
+            const int64_t off = c - (int64_t)r * chunks_per_shard;
+            v[u] = __ldcs(reinterpret_cast<const uint4*>(src.p[r] + off * 8));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) reinterpret_cast<uint4*>(dst)[i + u * stride] = v[u];
+    }
+    for (; i < total; i += stride) {
+        const int r = (int)(i / chunks_per_shard);
+        const int64_t off = i - (int64_t)r * chunks_per_shard;
+        reinterpret_cast<uint4*>(dst)[i] = __ldcs(reinterpret_cast<const uint4*>(src.p[r] + off * 8));
+    }
+}
+
+// Scalar path for any S or alignment.
+__global__ void __launch_bounds__(512) shard_gather_scalar(ShardPtrs src, int dp, int64_t S, uint16_t* __restrict__ dst) {
+    const int64_t total = S * dp;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int r = (int)(i / S);
+        dst[i] = src.p[r][i - (int64_t)r * S];
+    }
+}
+
+int launch_shard_gather(const uint16_t* const* shards, int dp, int64_t S, uint16_t* dst, cudaStream_t st,
+                        int num_sms) {
+    if (!shards || !dst) return set_error(DLO_ERR_INVALID_ARG, "shard gather: null pointer");
+    if (dp < 1 || dp > kMaxGatherShards) return set_error(DLO_ERR_INVALID_ARG, "shard gather: dp %d not in [1, 64]", dp);
+    if (S < 0) return set_error(DLO_ERR_INVALID_ARG, "shard gather: negative S");
+    if (S == 0) return DLO_OK;
+    ShardPtrs sp{};
+    bool vec = (S % 8 == 0) && (reinterpret_cast<uintptr_t>(dst) % 16 == 0);
+    for (int r = 0; r < dp; ++r) {
+        if (!shards[r]) return set_error(DLO_ERR_INVALID_ARG, "shard gather: shard %d is null", r);
+        sp.p[r] = shards[r];
+        vec = vec && (reinterpret_cast<uintptr_t>(shards[r]) % 16 == 0);
+    }
+    const int grid = num_sms * 2;
+    if (vec)
+        shard_gather_vec<<<grid, 512, 0, st>>>(sp, dp, S, dst);
+    else
+        shard_gather_scalar<<<grid, 512, 0, st>>>(sp, dp, S, dst);
+    DLO_CUDA_TRY(cudaGetLastError());
+    return DLO_OK;
+}
+
+// ------------------------------------------------------------------ adaLN modulation
+
+constexpr int kAdaMaxC = 1024;
+constexpr int kAdaRChunk = 4;
+
+// One warp per output feature n: mod[r, n] = sum_c ada_w[n, c] * SiLU(cond[r, c]) + ada_b[n].
+// SiLU(cond) for up to kAdaRChunk requests is staged in shared memory.
+__global__ void __launch_bounds__(256) adaln_gemv(const uint16_t* __restrict__ W, const uint16_t* __restrict__ b,
+                                                  const float* __restrict__ cond, int R, int C, int N,
+                                                  float* __restrict__ mod) {
+    __shared__ float sc[kAdaRChunk * kAdaMaxC];  // SiLU(cond) of up to kAdaRChunk requests
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = blockIdx.x * 8 + warp;
+    for (int r0 = 0; r0 < R; r0 += kAdaRChunk) {
+        const int rc = min(kAdaRChunk, R - r0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < rc * C; i += blockDim.x) {
+            const float c = cond[(size_t)(r0 + i / C) * C + i % C];
+            sc[i] = c / (1.0f + expf(-c));
+        }
+        __syncthreads();
+        if (n < N) {
+            float acc[kAdaRChunk] = {0.f, 0.f, 0.f, 0.f};
+            const uint16_t* wrow = W + (size_t)n * C;
+            for (int c0 = lane * 8; c0 < C; c0 += 256) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(wrow + c0));
+                const float wf[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                     bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+                for (int r = 0; r < kAdaRChunk; ++r) {
+                    if (r < rc) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) acc[r] = fmaf(wf[k], sc[r * C + c0 + k], acc[r]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kAdaRChunk; ++r) {
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+            }
+            if (lane == 0) {
+                const float bn = bf16_lo(b[n]);
+                for (int r = 0; r < rc; ++r) mod[(size_t)(r0 + r) * N + n] = acc[r] + bn;
+            }
+        }
+    }
+}
+
+int launch_adaln(const uint16_t* ada_w, const uint16_t* ada_b, const float* cond, int R, int C, int N, float* mod,
+                 cudaStream_t st) {
+    if (!ada_w || !ada_b || !cond || !mod) return set_error(DLO_ERR_INVALID_ARG, "adaln: null pointer");
+    if (R <= 0 || C <= 0 || N <= 0) return set_error(DLO_ERR_INVALID_ARG, "adaln: non-positive size");
+    if (C % 8) return set_error(DLO_ERR_ALIGNMENT, "adaln: cond_dim must be a multiple of 8");
+    if (C > kAdaMaxC) return set_error(DLO_ERR_SHAPE, "adaln: cond_dim %d above %d", C, kAdaMaxC);
+    adaln_gemv<<<(N + 7) / 8, 256, 0, st>>>(ada_w, ada_b, cond, R, C, N, mod);
+    DLO_CUDA_TRY(cudaGetLastError());
+    return DLO_OK;
+}
+
+// ------------------------------------------------------------------ LayerNorm + modulate
+
+constexpr int kLnThreads = 256;
+constexpr int kLnMaxVec = 8;  // float4 per thread: hidden <= 8192
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kLnThreads / 32; ++w) t += red[w];
+    return t;
+}
+
+// One CTA per token row; the row stays in registers between the two passes.
+__global__ void __launch_bounds__(kLnThreads) ln_modulate(const float* __restrict__ x, const float* __restrict__ shift,
+                                                          const float* __restrict__ scale, int mod_stride, int T,
+                                                          int hidden, uint16_t* __restrict__ u) {
+    __shared__ float red[kLnThreads / 32];
+    const int row = blockIdx.x;
+    const int req = row / T;
+    const int nvec = hidden / 4;
+    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * hidden);
+    float4 v[kLnMaxVec];
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < kLnMaxVec; ++k) {
+        const int i = threadIdx.x + k * kLnThreads;
+        if (i < nvec) {
+            v[k] = xr[i];
+            s += (v[k].x + v[k].y) + (v[k].z + v[k].w);
+        }
+    }
+    const float mean = block_sum(s, red) / (float)hidden;
+    float q = 0.f;
+#pragma unroll
+    for (int k = 0; k < kLnMaxVec; ++k) {
+        const int i = threadIdx.x + k * kLnThreads;
+        if (i < nvec) {
+            const float a = v[k].x - mean, b = v[k].y - mean, c = v[k].z - mean, d = v[k].w - mean;
+            q += (a * a + b * b) + (c * c + d * d);
+        }
+    }
+    const float var = block_sum(q, red) / (float)hidden;
+    const float rstd = 1.0f / sqrtf(var + 1e-6f);
+    const float4* shr = reinterpret_cast<const float4*>(shift + (size_t)req * mod_stride);
+    const float4* scr = reinterpret_cast<const float4*>(scale + (size_t)req * mod_stride);
+    uint2* ur = reinterpret_cast<uint2*>(u + (size_t)row * hidden);
+#pragma unroll
+    for (int k = 0; k < kLnMaxVec; ++k) {
+        const int i = threadIdx.x + k * kLnThreads;
+        if (i < nvec) {
+            const float4 sh = shr[i], sc = scr[i];
+            uint2 o;
+            o.x = pack_bf16x2((v[k].x - mean) * rstd * (1.f + sc.x) + sh.x, (v[k].y - mean) * rstd * (1.f + sc.y) + sh.y);
+            o.y = pack_bf16x2((v[k].z - mean) * rstd * (1.f + sc.z) + sh.z, (v[k].w - mean) * rstd * (1.f + sc.w) + sh.w);
+            ur[i] = o;
+        }
+    }
+}
+
+int launch_ln_modulate(const float* x, const float* shift, const float* scale, int mod_stride, int R, int T,
+                       int hidden, uint16_t* u, cudaStream_t st) {
+    if (!x || !shift || !scale || !u) return set_error(DLO_ERR_INVALID_ARG, "ln_modulate: null pointer");
+    if (R <= 0 || T <= 0 || hidden <= 0) return set_error(DLO_ERR_INVALID_ARG, "ln_modulate: non-positive size");
+    if (hidden % 8 || mod_stride % 4) return set_error(DLO_ERR_ALIGNMENT, "ln_modulate: hidden % 8, mod_stride % 4");
+    if (hidden > kLnThreads * kLnMaxVec * 4) return set_error(DLO_ERR_SHAPE, "ln_modulate: hidden %d above 8192", hidden);
+    const long rows = (long)R * T;
+    if (rows > 0x7FFFFFFFL) return set_error(DLO_ERR_SHAPE, "ln_modulate: too many rows");
+    ln_modulate<<<(unsigned)rows, kLnThreads, 0, st>>>(x, shift, scale, mod_stride, T, hidden, u);
+    DLO_CUDA_TRY(cudaGetLastError());
+    return DLO_OK;
+}
+
+}  // namespace dlo

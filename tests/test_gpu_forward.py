@@ -1,0 +1,253 @@
+"""The streamed forward through the C ABI against the oracle, and the
+placement invariants the pages fix ("vLLM-Omni 发布 Distributed Layerwise
+Offload…": identical outputs across placement strategies in its validation
+and B300 sections; two slots of the largest block in section 3)."""
+import numpy as np
+import pytest
+import torch
+
+import layerwise_weight_offloaded_gb300 as dlo
+import synthetic
+from layerwise_weight_offloaded_gb300.pinned import PinnedShards
+from oracle import dit
+
+from _workload import assert_close_rel_max, oracle_params, param_source, spec_tuple, zero_gates
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2  # max|gpu - ref| <= 2e-2 * max|ref| (bf16 weights, fp32 accumulation)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from layerwise_weight_offloaded_gb300 import build
+    build.build()
+    torch.cuda.init()
+    yield
+
+
+class Run:
+    """A handle over pinned shards plus the forward it computes."""
+
+    def __init__(self, specs, dp, seed=0, flags=dlo.DLO_FILL_AUTO, transform=None, contiguous=False):
+        self.specs = specs
+        self.src = param_source(seed, transform)
+        self.ps = PinnedShards(specs, dp, self.src, contiguous=contiguous)
+        self.h = dlo.dlo_create(specs, dp, self.ps.ptrs, flags)
+
+    def forward(self, x_np, c_np):
+        R, T, hd = x_np.shape
+        x = torch.from_numpy(x_np).cuda()
+        c = torch.from_numpy(c_np).cuda()
+        dlo.dlo_forward(self.h, x, c, R, T, torch.cuda.current_stream())
+        dlo.dlo_synchronize(self.h, 120000)
+        return x.cpu().numpy()
+
+    def close(self):
+        dlo.dlo_destroy(self.h)
+        self.h = 0
+
+
+def inputs(cfg_or_shape, seed=0):
+    R, T, h, C = cfg_or_shape
+    return synthetic.tokens(seed, R, T, h), synthetic.cond(seed, R, C)
+
+
+def check_vs_oracle(specs, x, c, got, src, what):
+    ref = dit.forward(x, c, oracle_params(specs, src), specs[0][1])
+    assert_close_rel_max(got, ref, TOL, what)
+    # the stricter check the residual stream would hide: the change each stack makes
+    assert_close_rel_max(got - x, ref - x, TOL, what + " (delta)")
+    return ref
+
+
+def test_tiny_full_forward_vs_oracle():
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * cfg.blocks
+    run = Run(specs, cfg.dp_size, cfg.seed)
+    try:
+        x, c = inputs((cfg.requests, cfg.tokens, cfg.hidden, cfg.cond_dim), cfg.seed)
+        got = run.forward(x, c)
+        check_vs_oracle(specs, x, c, got, run.src, "tiny")
+        st = dlo.dlo_get_stats(run.h)
+        n = dlo.dlo_block_numel(specs[0])
+        assert st["slot_bytes"] == dlo.dlo_shard_numel(n, cfg.dp_size) * cfg.dp_size * 2
+        assert st["device_weight_high_water"] == 2 * st["slot_bytes"]
+    finally:
+        run.close()
+
+
+def test_ragged_multi_request_and_mixed_blocks_vs_oracle():
+    """R=3 requests of T=100 tokens; blocks of different MLP width / head dim:
+    the slots are sized to the largest block."""
+    specs = [(256, 4, 1024, 256), (256, 2, 512, 256), (256, 4, 1536, 256), (256, 2, 256, 256)]
+    run = Run(specs, 3, seed=11)
+    try:
+        x, c = inputs((3, 100, 256, 256), 5)
+        got = run.forward(x, c)
+        check_vs_oracle(specs, x, c, got, run.src, "mixed")
+        n_max = max(dlo.dlo_block_numel(s) for s in specs)
+        st = dlo.dlo_get_stats(run.h)
+        assert st["slot_bytes"] == dlo.dlo_shard_numel(n_max, 3) * 3 * 2
+    finally:
+        run.close()
+
+
+def test_streamed_equals_resident_and_dp_invariant():
+    """Placement changes no output bit: streamed vs all-resident, every dp,
+    copy-engine vs zero-copy fill, separate vs contiguous shard allocations."""
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * 6
+    x, c = inputs((2, 200, cfg.hidden, cfg.cond_dim), 3)
+    outs = {}
+    for name, dp, flags, contiguous in [
+        ("stream-dp4-memcpy", 4, dlo.DLO_FILL_MEMCPY, False),
+        ("resident-dp4", 4, dlo.DLO_FILL_MEMCPY | dlo.DLO_RESIDENT, False),
+        ("stream-dp4-zerocopy", 4, dlo.DLO_FILL_ZEROCOPY, False),
+        ("stream-dp1", 1, dlo.DLO_FILL_MEMCPY, False),
+        ("stream-dp2", 2, dlo.DLO_FILL_ZEROCOPY, False),
+        ("stream-dp8-contig", 8, dlo.DLO_FILL_MEMCPY, True),
+        ("stream-dp7", 7, dlo.DLO_FILL_AUTO, False),
+    ]:
+        run = Run(specs, dp, 0, flags, contiguous=contiguous)
+        try:
+            outs[name] = run.forward(x, c)
+            again = run.forward(x, c)
+            assert np.array_equal(outs[name], again), name + " not deterministic"
+        finally:
+            run.close()
+    base = outs["stream-dp4-memcpy"]
+    for name, o in outs.items():
+        assert np.array_equal(o.view(np.uint32), base.view(np.uint32)), name
+
+
+def test_zero_gates_identity_bit_exact():
+    """ada_w = 0 and zero gate biases make every block the identity: x comes back unchanged."""
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * cfg.blocks
+    run = Run(specs, cfg.dp_size, 0, transform=zero_gates(cfg.hidden))
+    try:
+        x, c = inputs((2, 77, cfg.hidden, cfg.cond_dim), 9)
+        got = run.forward(x, c)
+        assert np.array_equal(got, x)
+    finally:
+        run.close()
+
+
+def test_requests_batched_equal_alone():
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * 2
+    run = Run(specs, 2, 4)
+    try:
+        x, c = inputs((3, 96, cfg.hidden, cfg.cond_dim), 2)
+        both = run.forward(x, c)
+        one = run.forward(np.ascontiguousarray(x[1:2]), np.ascontiguousarray(c[1:2]))
+        assert np.array_equal(both[1], one[0])
+    finally:
+        run.close()
+
+
+def test_forward_host_equals_device_forward():
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * cfg.blocks
+    run = Run(specs, cfg.dp_size)
+    try:
+        x, c = inputs((1, cfg.tokens, cfg.hidden, cfg.cond_dim), 1)
+        dev = run.forward(x, c)
+        xh = torch.from_numpy(x.copy()).pin_memory()
+        ch = torch.from_numpy(c.copy())
+        dlo.dlo_forward_host(run.h, xh, ch, 1, cfg.tokens, torch.cuda.current_stream())
+        assert np.array_equal(xh.numpy(), dev)
+    finally:
+        run.close()
+
+
+def test_weight_footprint_independent_of_depth():
+    """Two slots of the largest block whatever the depth (section 3): L=4 and L=40."""
+    cfg = synthetic.get_config("tiny")
+    spec = spec_tuple(cfg)
+    seen = []
+    for L in (4, 40):
+        run = Run([spec] * L, cfg.dp_size, flags=dlo.DLO_FILL_MEMCPY)
+        try:
+            x, c = inputs((1, 64, cfg.hidden, cfg.cond_dim), 0)
+            run.forward(x, c)
+            st = dlo.dlo_get_stats(run.h)
+            assert st["device_weight_high_water"] == 2 * st["slot_bytes"]
+            assert st["fills"] == L
+            seen.append((st["slot_bytes"], st["device_weight_high_water"]))
+            assert st["host_shard_bytes"] == L * st["slot_bytes"]
+        finally:
+            run.close()
+    assert seen[0] == seen[1]
+
+
+def test_profile_counts_every_kernel():
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * cfg.blocks
+    run = Run(specs, cfg.dp_size, flags=dlo.DLO_FILL_ZEROCOPY | dlo.DLO_PROFILE)
+    try:
+        x, c = inputs((1, cfg.tokens, cfg.hidden, cfg.cond_dim), 0)
+        run.forward(x, c)
+        kt = dlo.dlo_get_kernel_times(run.h)
+        L = cfg.blocks
+        want = {"fill": L, "adaln": L, "ln_modulate": 2 * L, "gemm_qkv": L, "attention": L, "gemm_proj": L,
+                "gemm_fc1": L, "gemm_fc2": L}
+        assert {k: v[1] for k, v in kt.items()} == want
+        assert all(v[0] > 0 for v in kt.values())
+    finally:
+        run.close()
+
+
+def test_host_side_timeout_and_error_state():
+    """A bounded host wait that expires reports DLO_ERR_TIMEOUT and fails the handle closed."""
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * 8
+    run = Run(specs, cfg.dp_size, flags=dlo.DLO_FILL_MEMCPY)
+    try:
+        x = torch.from_numpy(synthetic.tokens(0, 4, 2048, cfg.hidden)).cuda()
+        c = torch.from_numpy(synthetic.cond(0, 4, cfg.cond_dim)).cuda()
+        s = torch.cuda.current_stream()
+        torch.cuda._sleep(int(2e9))  # keeps the stream busy (about a second) ahead of the forward
+        dlo.dlo_forward(run.h, x, c, 4, 2048, s)
+        with pytest.raises(dlo.DloError) as e:
+            dlo.dlo_synchronize(run.h, 0)
+        assert e.value.status == dlo.DLO_ERR_TIMEOUT
+        with pytest.raises(dlo.DloError) as e:
+            dlo.dlo_forward(run.h, x, c, 4, 2048, s)
+        assert e.value.status == dlo.DLO_ERR_STATE
+        torch.cuda.synchronize()
+    finally:
+        run.close()
+
+
+def test_invalid_forward_arguments():
+    cfg = synthetic.get_config("tiny")
+    run = Run([spec_tuple(cfg)], 2)
+    try:
+        x = torch.zeros(1, 8, cfg.hidden, device="cuda")
+        c = torch.zeros(1, cfg.cond_dim, device="cuda")
+        for R, T in ((0, 8), (1, 0), (70000, 1)):
+            with pytest.raises(dlo.DloError):
+                dlo.dlo_forward(run.h, x, c, R, T)
+        with pytest.raises(dlo.DloError) as e:
+            dlo.dlo_forward(run.h, x.view(-1)[1:].data_ptr(), c, 1, 4)
+        assert e.value.status == dlo.DLO_ERR_ALIGNMENT
+        dlo.dlo_forward(run.h, x, c, 1, 8)  # still usable after rejected calls
+        dlo.dlo_synchronize(run.h, 60000)
+    finally:
+        run.close()
+    with pytest.raises(dlo.DloError):
+        dlo.dlo_create([spec_tuple(cfg), (512, 8, 1024, 256)], 2, [0] * 4)
+
+
+def test_t2i_full_depth_vs_oracle():
+    """The 1024x1024 text-to-image workload (16 blocks, 4096 tokens, dp 4) at full depth."""
+    cfg = synthetic.get_config("t2i")
+    specs = [spec_tuple(cfg)] * cfg.blocks
+    run = Run(specs, cfg.dp_size, cfg.seed)
+    try:
+        x, c = inputs((cfg.requests, cfg.tokens, cfg.hidden, cfg.cond_dim), cfg.seed)
+        got = run.forward(x, c)
+        check_vs_oracle(specs, x, c, got, run.src, "t2i")
+    finally:
+        run.close()

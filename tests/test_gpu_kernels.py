@@ -1,0 +1,216 @@
+"""Each kernel of one block against the oracle's routine, through the C ABI.
+
+Sizes span several tiles with ragged tails; inputs are seeded.  Tolerances
+follow from the arithmetic: outputs stored as bf16 carry a rounding error of
+at most 2^-9 relative (round to nearest even), fp32 accumulation adds far
+less at these K; attention also rounds its softmax weights to bf16 before the
+P.V product.
+"""
+import numpy as np
+import pytest
+import torch
+
+import layerwise_weight_offloaded_gb300 as dlo
+import synthetic
+from oracle import dit, shards
+from layerwise_weight_offloaded_gb300.pinned import PinnedShards
+
+from _workload import bf16_bits_to_f64, param_source, spec_tuple
+
+pytestmark = pytest.mark.gpu
+BF16_REL = 2.0 ** -8  # twice the RNE bound, for the fp32 rounding before it
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from layerwise_weight_offloaded_gb300 import build
+    build.build()
+    torch.cuda.init()
+    yield
+    dlo.dlo_op_check()
+
+
+def bf16_tensor(seed, tid, shape, std, device="cuda"):
+    bits = synthetic.normal_bf16_bits(seed, tid, shape, std)
+    return torch.from_numpy(bits.view(np.int16)).to(device), bits
+
+
+def f32_tensor(seed, tid, shape, std=1.0, device="cuda"):
+    a = synthetic.normal_f32(seed, tid, shape, std)
+    return torch.from_numpy(a).to(device), a
+
+
+def to_bits(t):
+    return t.cpu().numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------- fill
+
+@pytest.mark.parametrize("spec,dp", [((64, 1, 8, 8), 1), ((64, 1, 8, 8), 5), ((64, 1, 8, 8), 8),
+                                     ((256, 4, 1024, 256), 4), ((128, 1, 72, 16), 3)])
+@pytest.mark.parametrize("mode", [dlo.DLO_FILL_MEMCPY, dlo.DLO_FILL_ZEROCOPY])
+def test_slot_fill_bit_exact(spec, dp, mode):
+    """The rebuilt slot equals the rank-ordered concatenation of the shards."""
+    L = 3
+    ps = PinnedShards([spec] * L, dp, param_source(7))
+    h = dlo.dlo_create([spec] * L, dp, ps.ptrs, mode)
+    try:
+        st = dlo.dlo_get_stats(h)
+        n = dlo.dlo_block_numel(spec)
+        S = dlo.dlo_shard_numel(n, dp)
+        assert st["slot_bytes"] == dp * S * 2
+        for b in range(L):
+            got = np.empty(dp * S, np.uint16)
+            dlo.dlo_debug_fill_and_read(h, b, b % 2, got, got.nbytes)
+            want = shards.gather([ps.shard_numpy(b, r) for r in range(dp)])
+            assert np.array_equal(got, want)
+            flat = np.concatenate([synthetic.weight_bits(7, b, i, s).reshape(-1)
+                                   for i, (_, s) in enumerate(dit.param_shapes(spec[0], spec[2], spec[3]))])
+            assert np.array_equal(got[:n], flat) and not got[n:].any()
+    finally:
+        dlo.dlo_destroy(h)
+
+
+def test_shard_gather_op_misaligned():
+    """Scalar path: odd S and odd device offsets of the shards."""
+    S, dp = 1001, 3
+    host = torch.empty(dp * S + 8, dtype=torch.int16, pin_memory=True)
+    host.copy_(torch.arange(dp * S + 8, dtype=torch.int32).to(torch.int16))
+    shards_p = [host.data_ptr() + 2 * (1 + r * S) for r in range(dp)]  # 2-byte aligned only
+    dst = torch.zeros(dp * S, dtype=torch.int16, device="cuda")
+    dlo.dlo_op_shard_gather(shards_p, dp, S, dst)
+    dlo.dlo_op_check()
+    assert torch.equal(dst.cpu(), host[1:1 + dp * S])
+
+
+# ---------------------------------------------------------------- adaLN
+
+@pytest.mark.parametrize("R,C,h", [(1, 256, 64), (4, 256, 256), (5, 8, 64), (2, 1024, 128), (3, 256, 1536)])
+def test_adaln_vs_oracle(R, C, h):
+    N = 6 * h
+    w, wb = bf16_tensor(1, 1, (N, C), 0.05)
+    b, bb = bf16_tensor(1, 2, (N,), 0.1)
+    c, cn = f32_tensor(1, 3, (R, C))
+    mod = torch.empty(R, N, device="cuda")
+    dlo.dlo_op_adaln(w, b, c, R, C, N, mod)
+    dlo.dlo_op_check()
+    ref = dit.adaln_modulation(bf16_bits_to_f64(wb).reshape(N, C), bf16_bits_to_f64(bb), cn)
+    np.testing.assert_allclose(mod.cpu().numpy(), ref, rtol=1e-5, atol=1e-6 * C)
+
+
+# ---------------------------------------------------------------- LayerNorm + modulate
+
+@pytest.mark.parametrize("R,T,h", [(1, 1, 64), (2, 37, 256), (1, 130, 1536), (3, 5, 200), (1, 9, 8192)])
+def test_ln_modulate_vs_oracle(R, T, h):
+    x, xn = f32_tensor(2, 1, (R * T, h), 2.0)
+    x += 0.5
+    xn = x.cpu().numpy()
+    mod, modn = f32_tensor(2, 2, (R, 6 * h), 0.3)
+    u = torch.empty(R * T, h, dtype=torch.int16, device="cuda")
+    dlo.dlo_op_ln_modulate(x, mod[:, 3 * h:], mod[:, 4 * h:], 6 * h, R, T, h, u)
+    dlo.dlo_op_check()
+    got = bf16_bits_to_f64(to_bits(u)).reshape(R * T, h)
+    req = np.arange(R * T) // T
+    ref = dit.modulate(dit.layer_norm(xn), modn[req, 3 * h:4 * h], modn[req, 4 * h:5 * h])
+    assert np.all(np.abs(got - ref) <= BF16_REL * np.abs(ref) + 1e-5 * np.abs(ref).max())
+
+
+def test_ln_modulate_constant_rows_give_shift():
+    """Closed form: a constant row normalises to 0, so u = bf16(shift) exactly."""
+    R, T, h = 2, 3, 256
+    x = torch.full((R * T, h), 2.75, device="cuda")
+    mod, modn = f32_tensor(3, 1, (R, 6 * h), 0.5)
+    u = torch.empty(R * T, h, dtype=torch.int16, device="cuda")
+    dlo.dlo_op_ln_modulate(x, mod, mod[:, h:], 6 * h, R, T, h, u)
+    dlo.dlo_op_check()
+    want = torch.from_numpy(np.repeat(modn[:, :h], T, axis=0)).to(torch.bfloat16).view(torch.int16)
+    assert torch.equal(u.cpu(), want)
+
+
+# ---------------------------------------------------------------- linear (tcgen05 GEMM)
+
+GEMM_SHAPES = [(128, 256, 64), (200, 136, 72), (1000, 768, 256), (333, 1032, 520), (2048, 4608, 256),
+               (4096, 1536, 1536), (130, 8, 8)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+@pytest.mark.parametrize("epi", [dlo.DLO_EPI_BIAS, dlo.DLO_EPI_BIAS_GELU, dlo.DLO_EPI_GATED_RESIDUAL])
+def test_linear_vs_oracle(M, N, K, epi):
+    A, Ab = bf16_tensor(4, 1, (M, K), 1.0)
+    W, Wb = bf16_tensor(4, 2, (N, K), 0.05)
+    bias, bb = bf16_tensor(4, 3, (N,), 0.1)
+    lin = dit.linear(bf16_bits_to_f64(Ab).reshape(M, K), bf16_bits_to_f64(Wb).reshape(N, K), bf16_bits_to_f64(bb))
+    if epi == dlo.DLO_EPI_GATED_RESIDUAL:
+        T = max(1, M // 3)
+        R = (M + T - 1) // T
+        gate, gn = f32_tensor(4, 4, (R, 3 * N), 0.3)
+        x, xn = f32_tensor(4, 5, (M, N))
+        dlo.dlo_op_linear(epi, A, W, bias, M, N, K, x, gate[:, N:], 3 * N, T)
+        dlo.dlo_op_check()
+        ref = xn + gn[np.arange(M) // T, N:2 * N] * lin
+        got = x.cpu().numpy()
+        np.testing.assert_allclose(got, ref, rtol=0, atol=2e-5 * np.abs(ref).max())
+    else:
+        out = torch.empty(M, N, dtype=torch.int16, device="cuda")
+        dlo.dlo_op_linear(epi, A, W, bias, M, N, K, out)
+        dlo.dlo_op_check()
+        ref = dit.gelu_tanh(lin) if epi == dlo.DLO_EPI_BIAS_GELU else lin
+        got = bf16_bits_to_f64(to_bits(out)).reshape(M, N)
+        err = np.abs(got - ref)
+        assert np.all(err <= BF16_REL * np.abs(ref) + 2e-5 * np.abs(ref).max()), err.max()
+
+
+def test_linear_rows_independent_of_batch():
+    """Each output row is computed the same way whatever M is: bit-identical."""
+    K, N = 512, 768
+    A, _ = bf16_tensor(5, 1, (1000, K), 1.0)
+    W, _ = bf16_tensor(5, 2, (N, K), 0.05)
+    bias, _ = bf16_tensor(5, 3, (N,), 0.1)
+    big = torch.empty(1000, N, dtype=torch.int16, device="cuda")
+    small = torch.empty(100, N, dtype=torch.int16, device="cuda")
+    dlo.dlo_op_linear(dlo.DLO_EPI_BIAS, A, W, bias, 1000, N, K, big)
+    dlo.dlo_op_linear(dlo.DLO_EPI_BIAS, A[300:400].contiguous(), W, bias, 100, N, K, small)
+    dlo.dlo_op_check()
+    assert torch.equal(big[300:400], small)
+
+
+# ---------------------------------------------------------------- attention
+
+@pytest.mark.parametrize("R,T,H,d", [(1, 64, 1, 64), (2, 100, 3, 64), (1, 257, 2, 128), (1, 1024, 4, 128),
+                                     (3, 65, 2, 128), (1, 2048, 2, 64)])
+def test_attention_vs_oracle(R, T, H, d):
+    h = H * d
+    qkv, qb = bf16_tensor(6, T, (R * T, 3 * h), 1.0)
+    o = torch.empty(R * T, h, dtype=torch.int16, device="cuda")
+    dlo.dlo_op_attention(qkv, R, T, H, d, o)
+    dlo.dlo_op_check()
+    got = bf16_bits_to_f64(to_bits(o)).reshape(R, T, h)
+    q = bf16_bits_to_f64(qb).reshape(R, T, 3 * h)
+    for r in range(R):
+        ref = dit.attention(q[r, :, :h], q[r, :, h:2 * h], q[r, :, 2 * h:], H)
+        err = np.abs(got[r] - ref)
+        assert np.all(err <= BF16_REL * np.abs(ref) + 8e-3 * np.abs(ref).max()), err.max()
+
+
+def test_attention_single_token_returns_v():
+    """Closed form: one key gets softmax weight exactly 1, so O = V bit for bit."""
+    R, T, H, d = 3, 1, 4, 64
+    qkv, qb = bf16_tensor(7, 1, (R * T, 3 * H * d), 1.0)
+    o = torch.empty(R * T, H * d, dtype=torch.int16, device="cuda")
+    dlo.dlo_op_attention(qkv, R, T, H, d, o)
+    dlo.dlo_op_check()
+    assert torch.equal(o, qkv[:, 2 * H * d:])
+
+
+def test_attention_zero_queries_give_mean_of_v():
+    """Closed form: zero queries weight every key equally, O = column mean of V."""
+    R, T, H, d = 1, 300, 2, 128
+    qkv, qb = bf16_tensor(8, 1, (T, 3 * H * d), 1.0)
+    qkv[:, :H * d] = 0
+    o = torch.empty(T, H * d, dtype=torch.int16, device="cuda")
+    dlo.dlo_op_attention(qkv, R, T, H, d, o)
+    dlo.dlo_op_check()
+    v = bf16_bits_to_f64(to_bits(qkv[:, 2 * H * d:])).reshape(T, H * d)
+    got = bf16_bits_to_f64(to_bits(o)).reshape(T, H * d)
+    ref = np.broadcast_to(v.mean(0), got.shape)
+    assert np.all(np.abs(got - ref) <= BF16_REL * np.abs(ref) + 1e-3)

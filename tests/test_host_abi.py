@@ -1,0 +1,136 @@
+"""Host side of the C ABI (no GPU): the library loads, exports every symbol the
+header declares, and its shard layout matches the oracle bit for bit."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import layerwise_weight_offloaded_gb300 as dlo
+from layerwise_weight_offloaded_gb300 import build as dlo_build
+from oracle import dit, shards
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    dlo_build.build()
+    yield
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "dlo.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dlo_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_symbols_are_exported():
+    import ctypes
+    L = ctypes.CDLL(dlo.LIB_PATH)
+    declared = _declared_symbols()
+    assert len(declared) >= 20
+    missing = [s for s in declared if not hasattr(L, s)]
+    assert not missing, missing
+    assert sorted(dlo.EXPORTED) == declared
+
+
+def test_library_exports_nothing_undeclared():
+    """Only the C ABI is visible (internal C++ symbols are hidden)."""
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", dlo.LIB_PATH], capture_output=True, text=True).stdout
+    ours = sorted({l.split()[-1] for l in out.splitlines() if l.split()[-1].startswith("dlo")})
+    assert ours == _declared_symbols()
+
+
+SPECS = [(64, 1, 8, 8), (256, 4, 1024, 256), (1536, 24, 6144, 256), (128, 1, 72, 16), (384, 3, 200, 24)]
+
+
+@pytest.mark.parametrize("spec", SPECS)
+def test_block_numel_and_param_table_match_oracle(spec):
+    h, H, m, C = spec
+    assert dlo.dlo_block_numel(spec) == dit.block_numel(h, m, C)
+    offs, nums = dlo.dlo_param_table(spec)
+    table = dit.param_table(h, m, C)
+    assert offs == [off for _, off, _ in table]
+    assert nums == [int(np.prod(shape)) for _, _, shape in table]
+    assert all(o % 8 == 0 for o in offs)  # every parameter starts 16-byte aligned
+
+
+def test_shard_numel_matches_oracle():
+    for n in list(range(0, 50)) + [10 ** 9 + 7, 2 ** 40 + 3]:
+        for dp in range(1, 12):
+            assert dlo.dlo_shard_numel(n, dp) == shards.shard_numel(n, dp)
+
+
+@pytest.mark.parametrize("spec", [(64, 1, 8, 8), (128, 1, 72, 16), (256, 4, 1024, 256)])
+def test_pack_block_bit_exact_vs_oracle(spec):
+    import synthetic
+    h, H, m, C = spec
+    n = dit.block_numel(h, m, C)
+    table = dit.param_table(h, m, C)
+    flat = synthetic.normal_bf16_bits(5, 1, (n,), 0.02)
+    params = [np.ascontiguousarray(flat[off: off + int(np.prod(shape))]) for _, off, shape in table]
+    for dp in range(1, 10):
+        S = dlo.dlo_shard_numel(n, dp)
+        out = [np.full(S, 0xABCD, np.uint16) for _ in range(dp)]  # garbage must be overwritten
+        dlo.dlo_pack_block(spec, params, dp, out)
+        want = shards.pack(flat, dp)
+        for r in range(dp):
+            assert np.array_equal(out[r], want[r]), (dp, r)
+        assert np.array_equal(shards.unpack(out, n), flat)
+
+
+def test_pack_padding_only_shards():
+    """dp larger than needed leaves whole trailing shards as zero padding."""
+    spec = (64, 1, 8, 8)
+    n = dlo.dlo_block_numel(spec)
+    dp = 64
+    S = dlo.dlo_shard_numel(n, dp)
+    flat = np.arange(1, n + 1, dtype=np.uint64).astype(np.uint16) | 1
+    table = dit.param_table(64, 8, 8)
+    params = [np.ascontiguousarray(flat[off: off + int(np.prod(shape))]) for _, off, shape in table]
+    out = [np.full(S, 0xFFFF, np.uint16) for _ in range(dp)]
+    dlo.dlo_pack_block(spec, params, dp, out)
+    g = np.concatenate(out)
+    assert np.array_equal(g[:n], flat) and not g[n:].any()
+
+
+@pytest.mark.parametrize("spec,status", [
+    ((0, 1, 8, 8), dlo.DLO_ERR_INVALID_ARG),
+    ((64, 1, 8, 12), dlo.DLO_ERR_ALIGNMENT),
+    ((68, 1, 8, 8), dlo.DLO_ERR_ALIGNMENT),
+    ((96, 1, 8, 8), dlo.DLO_ERR_SHAPE),    # head dim 96
+    ((128, 3, 8, 8), dlo.DLO_ERR_SHAPE),   # heads do not divide hidden
+    ((64, 1, 8, 2048), dlo.DLO_ERR_SHAPE),  # cond_dim above 1024
+    ((16384, 128, 8, 8), dlo.DLO_ERR_SHAPE),
+])
+def test_spec_validation(spec, status):
+    with pytest.raises(dlo.DloError) as e:
+        dlo.dlo_validate_spec(spec)
+    assert e.value.status == status
+    assert dlo.dlo_last_error()
+
+
+def test_invalid_arguments():
+    with pytest.raises(dlo.DloError) as e:
+        dlo.dlo_shard_numel(10, 0)
+    assert e.value.status == dlo.DLO_ERR_INVALID_ARG
+    with pytest.raises(dlo.DloError):
+        dlo.dlo_shard_numel(-1, 2)
+    import ctypes
+    L = dlo.lib()
+    assert L.dlo_pack_block(None, None, 1, None) == dlo.DLO_ERR_INVALID_ARG
+    assert L.dlo_create(None, 1, 1, None, 0, None) == dlo.DLO_ERR_INVALID_ARG
+    assert L.dlo_forward(None, None, None, 1, 1, None) == dlo.DLO_ERR_INVALID_ARG
+    assert L.dlo_destroy(None) == dlo.DLO_OK
+    assert dlo.dlo_status_string(dlo.DLO_ERR_TIMEOUT) == "DLO_ERR_TIMEOUT"
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the CUDA library the binding raises; it never computes on the CPU."""
+    import layerwise_weight_offloaded_gb300._binding as B
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(B.DloLibraryMissing):
+        B.dlo_block_numel((64, 1, 8, 8))
