@@ -167,6 +167,8 @@ struct dlo_handle {
 
 namespace {
 
+constexpr double kZeroCopyMargin = 1.15;
+
 int fail(dlo_handle* h, int status) {
     if (h && status != DLO_OK) h->status = status;
     return status;
@@ -492,8 +494,11 @@ int dlo_create(const dlo_block_spec* specs, int32_t num_blocks, int32_t dp_size,
         mode = DLO_FILL_MEMCPY;
         h->st.h2d_memcpy_gbs = time_fill(h, DLO_FILL_MEMCPY, 3);
         if (mapped) {
+            // The gather kernel holds SM load slots while it waits on the host
+            // link, which slows the compute kernels it overlaps; the copy engine
+            // does not.  Keep the copy engine unless the kernel is clearly faster.
             h->st.h2d_zerocopy_gbs = time_fill(h, DLO_FILL_ZEROCOPY, 3);
-            if (h->st.h2d_zerocopy_gbs > h->st.h2d_memcpy_gbs) mode = DLO_FILL_ZEROCOPY;
+            if (h->st.h2d_zerocopy_gbs > kZeroCopyMargin * h->st.h2d_memcpy_gbs) mode = DLO_FILL_ZEROCOPY;
         }
         if ((e = cudaStreamSynchronize(h->copy)) != cudaSuccess) return bail(cuda_error(e, "fill timing"));
     }
