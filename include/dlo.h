@@ -266,6 +266,32 @@ int dlo_op_shard_gather(const uint16_t* const* shards, int32_t dp, int64_t S, ui
 /* Synchronises `stream` and reports (then clears) the single-op timeout flag. */
 int dlo_op_check(dlo_stream_t stream);
 
+/* ---------------- linear layer without any device allocation ----------------
+ * The pages have no counterpart of this entry point.
+ *
+ * Computes exactly what dlo_op_linear computes (same kernel, same arguments,
+ * same results) for callers that may not allocate device memory - a host
+ * framework that owns all device memory and gives its plugins a fixed
+ * workspace, a service under a hard device-memory cap, or a latency-critical
+ * path that cannot take the implicit device synchronisation cudaMalloc may
+ * perform.  dlo_op_linear allocates its timeout word with cudaMalloc on its
+ * first call; this one keeps that scratch in a static device array of 64
+ * 32-bit words (256 bytes) that every GPU loading the library holds until
+ * the process exits, and calls no allocating routine.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - One call needs one word of the array, whatever M, N and K are; sizes are
+ *     limited by the kernel's 32-bit tile coordinates (DLO_ERR_SHAPE beyond).
+ *   - Every call shares the array, which keeps the last call's contents: each
+ *     call clears the word on `stream` before its kernel runs, so calls that
+ *     overlap on the GPU (other streams, other host threads) race on it.
+ *   - status: optional device int32 (NULL = not wanted) that receives, on
+ *     `stream` after the kernel, 0 or the code of a bounded wait that expired.
+ * Asynchronous on `stream` like dlo_op_linear. */
+int dlo_op_linear_noalloc(int32_t epilogue, const uint16_t* A, const uint16_t* W, const uint16_t* bias,
+                          int32_t M, int32_t N, int32_t K, void* out, const float* gate, int32_t gate_stride,
+                          int32_t T, int32_t* status, dlo_stream_t stream);
+
 #if defined(__GNUC__)
 #pragma GCC visibility pop
 #endif

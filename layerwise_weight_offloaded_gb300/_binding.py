@@ -42,6 +42,7 @@ EXPORTED = (
     "dlo_last_error", "dlo_status_string", "dlo_create", "dlo_forward", "dlo_forward_host", "dlo_synchronize",
     "dlo_get_stats", "dlo_get_kernel_times", "dlo_debug_fill_and_read", "dlo_destroy", "dlo_op_adaln",
     "dlo_op_ln_modulate", "dlo_op_linear", "dlo_op_attention", "dlo_op_shard_gather", "dlo_op_check",
+    "dlo_op_linear_noalloc",
 )
 
 
@@ -94,6 +95,8 @@ _SIGS = {
     "dlo_op_attention": [_c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p],
     "dlo_op_shard_gather": [ctypes.POINTER(_c_p), _c_i32, _c_i64, _c_p, _c_p],
     "dlo_op_check": [_c_p],
+    "dlo_op_linear_noalloc": [_c_i32, _c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_i32, _c_i32, _c_p,
+                              _c_p],
 }
 
 
@@ -268,6 +271,13 @@ def dlo_op_attention(qkv, R: int, T: int, H: int, d: int, o, stream=None) -> Non
 def dlo_op_shard_gather(shards, dp: int, S: int, dst, stream=None) -> None:
     arr = (_c_p * dp)(*[_ptr(s) for s in shards])
     _check(lib().dlo_op_shard_gather(arr, dp, S, _ptr(dst), _stream(stream)))
+
+
+def dlo_op_linear_noalloc(epilogue: int, A, W, bias, M: int, N: int, K: int, out, gate=None,
+                          gate_stride: int = 0, T: int = 1, status=None, stream=None) -> None:
+    """dlo_op_linear with its scratch in a static device array: allocates nothing."""
+    _check(lib().dlo_op_linear_noalloc(epilogue, _ptr(A), _ptr(W), _ptr(bias), M, N, K, _ptr(out), _ptr(gate),
+                                       gate_stride, T, _ptr(status), _stream(stream)))
 
 
 def dlo_op_check(stream=None) -> None:

@@ -24,7 +24,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libdlo.so")
 
-SOURCES = ["dlo_host.cpp", "dlo_runtime.cu", "k_small.cu", "k_gemm.cu", "k_attention.cu"]
+SOURCES = ["dlo_host.cpp", "dlo_runtime.cu", "k_small.cu", "k_gemm.cu", "k_attention.cu", "dlo_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
           f"-I{INCLUDE}", f"-I{CSRC}", "--expt-relaxed-constexpr"]

@@ -1,0 +1,88 @@
+// dlo_op_linear_noalloc: the tcgen05 linear layer for callers that may not
+// allocate device memory.
+//
+// dlo_op_linear keeps the word its CTAs use to report an expired bounded wait
+// in device memory it allocates with cudaMalloc on its first call on a device.
+// Some callers cannot allow that: a host framework that owns all device memory
+// and hands its plugins a fixed workspace, a service running under a hard
+// device-memory cap, or a latency-critical path that cannot take the implicit
+// device-wide synchronisation cudaMalloc may perform.  This variant keeps that
+// scratch in a static device array instead, so a call allocates nothing.  It
+// has no counterpart in the pages.
+//
+// Set-up: the first call on each device looks up the array's device address
+// (cudaGetSymbolAddress, with that device current); make that first call before
+// any stream capture begins.
+//
+// Scratch: kNoallocScratchWords 32-bit words (256 bytes) in device memory that
+// every GPU which loads the library holds until the process exits.  One call
+// needs one word: word 0, the expired-wait code shared by the kernel's CTAs.
+// Every call shares the array and the word keeps the last call's contents, so
+// each call clears it first (on its stream); calls that overlap on the GPU
+// race on it.
+#include <mutex>
+
+#include "dlo_internal.h"
+
+namespace dlo {
+
+constexpr int kNoallocScratchWords = 64;
+constexpr int kNoallocWordsPerCall = 1;
+
+static __device__ __align__(256) int g_linear_noalloc_scratch[kNoallocScratchWords];
+
+// Device address of the scratch array on the current device.  The first call on
+// a device looks it up (cudaGetSymbolAddress, with that device current); the
+// name of the array in host code is only a host-side stand-in, never a device
+// address.
+static int noalloc_scratch(int** out) {
+    static int* addr[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    DLO_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return set_error(DLO_ERR_INVALID_ARG, "device index %d out of range", dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_linear_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_error(e, "cudaGetSymbolAddress(g_linear_noalloc_scratch)");
+        addr[dev] = static_cast<int*>(p);
+    }
+    *out = addr[dev];
+    return DLO_OK;
+}
+
+}  // namespace dlo
+
+using namespace dlo;
+
+extern "C" int dlo_op_linear_noalloc(int32_t epilogue, const uint16_t* A, const uint16_t* W, const uint16_t* bias,
+                                     int32_t M, int32_t N, int32_t K, void* out, const float* gate,
+                                     int32_t gate_stride, int32_t T, int32_t* status, dlo_stream_t stream) {
+    static_assert(kNoallocWordsPerCall <= kNoallocScratchWords, "scratch array too small for one call");
+    DeviceInfo d;
+    int rc = device_info(&d);
+    if (rc) return rc;
+    if (!A || !W || !bias || !out) return set_error(DLO_ERR_INVALID_ARG, "linear_noalloc: null pointer");
+    if (M <= 0 || N <= 0 || K <= 0) return set_error(DLO_ERR_INVALID_ARG, "linear_noalloc: non-positive size");
+    if (N % 8 || K % 8) return set_error(DLO_ERR_ALIGNMENT, "linear_noalloc: N and K must be multiples of 8");
+    // The scratch a call needs does not grow with M, N or K; sizes are bounded by
+    // the kernel's 32-bit tile coordinates instead.
+    if ((int64_t)M + 127 > 0x7FFFFFFF || (int64_t)N + 255 > 0x7FFFFFFF || (int64_t)K + 63 > 0x7FFFFFFF)
+        return set_error(DLO_ERR_SHAPE, "linear_noalloc: M, N or K too large for 32-bit tile coordinates");
+    if (reinterpret_cast<uintptr_t>(bias) % 16 || reinterpret_cast<uintptr_t>(out) % 16 ||
+        (gate && reinterpret_cast<uintptr_t>(gate) % 16) || (status && reinterpret_cast<uintptr_t>(status) % 4))
+        return set_error(DLO_ERR_ALIGNMENT, "linear_noalloc: bias, out and gate 16-byte, status 4-byte aligned");
+    int* scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch))) return rc;
+    CUtensorMap ta, tw[2];
+    if ((rc = encode_tmap_bf16(&ta, A, (uint64_t)K, (uint64_t)M, 128))) return rc;
+    if ((rc = encode_tmap_bf16(&tw[0], W, (uint64_t)K, (uint64_t)N, 128))) return rc;
+    if ((rc = encode_tmap_bf16(&tw[1], W, (uint64_t)K, (uint64_t)N, 256))) return rc;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    DLO_CUDA_TRY(cudaMemsetAsync(scratch, 0, kNoallocWordsPerCall * sizeof(int), s));
+    GemmArgs a{epilogue, M, N, K, bias, out, gate, gate_stride, T, scratch};
+    if ((rc = launch_gemm(ta, tw, a, s, d.num_sms))) return rc;
+    if (status) DLO_CUDA_TRY(cudaMemcpyAsync(status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, s));
+    return DLO_OK;
+}

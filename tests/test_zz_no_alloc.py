@@ -1,0 +1,93 @@
+"""dlo_op_linear_noalloc, the linear-layer entry point that allocates nothing.
+
+Callers that own all device memory (plugin hosts with a fixed workspace),
+that run under a hard memory cap, or that cannot take the device-wide
+synchronisation an allocation may cause, use this variant; its only scratch
+is a static device array.  Through the C ABI, two calls in a row must give
+what dlo_op_linear gives, within the tolerance of the GEMM parity tests, and
+report a clean status.  This file is collected last on purpose.
+"""
+import numpy as np
+import pytest
+import torch
+
+import layerwise_weight_offloaded_gb300 as dlo
+import synthetic
+
+pytestmark = pytest.mark.gpu
+BF16_REL = 2.0 ** -8
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from layerwise_weight_offloaded_gb300 import build
+    build.build()
+    torch.cuda.init()
+    yield
+
+
+def _bits(seed, tid, shape, std):
+    return torch.from_numpy(synthetic.normal_bf16_bits(seed, tid, shape, std).view(np.int16)).cuda()
+
+
+def _as_f64(t, epi):
+    if epi == dlo.DLO_EPI_GATED_RESIDUAL:
+        return t.cpu().numpy().astype(np.float64)
+    b = t.cpu().numpy().view(np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 136, 72), (1000, 768, 256), (2048, 4608, 256)])
+@pytest.mark.parametrize("epi", [dlo.DLO_EPI_BIAS, dlo.DLO_EPI_BIAS_GELU, dlo.DLO_EPI_GATED_RESIDUAL])
+def test_noalloc_matches_linear_twice(M, N, K, epi):
+    A = _bits(21, 1, (M, K), 1.0)
+    W = _bits(21, 2, (N, K), 0.05)
+    bias = _bits(21, 3, (N,), 0.1)
+    gated = epi == dlo.DLO_EPI_GATED_RESIDUAL
+    T = max(1, M // 3)
+    R = (M + T - 1) // T
+    gate = torch.from_numpy(synthetic.normal_f32(21, 4, (R, N), 0.3)).cuda() if gated else None
+    x0 = torch.from_numpy(synthetic.normal_f32(21, 5, (M, N))).cuda()
+
+    def fresh():
+        return x0.clone() if gated else torch.empty(M, N, dtype=torch.int16, device="cuda")
+
+    ref = fresh()
+    dlo.dlo_op_linear(epi, A, W, bias, M, N, K, ref, gate, N, T)
+    dlo.dlo_op_check()
+    want = _as_f64(ref, epi)
+    tol = BF16_REL * np.abs(want) + 2e-5 * np.abs(want).max()
+
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        out = fresh()
+        status.fill_(-1)
+        dlo.dlo_op_linear_noalloc(epi, A, W, bias, M, N, K, out, gate, N, T, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert np.all(np.abs(_as_f64(out, epi) - want) <= tol)
+
+
+def test_noalloc_second_call_leaves_free_memory_unchanged():
+    M, N, K = 512, 1024, 512
+    A, W, bias = _bits(22, 1, (M, K), 1.0), _bits(22, 2, (N, K), 0.05), _bits(22, 3, (N,), 0.1)
+    out = torch.empty(M, N, dtype=torch.int16, device="cuda")
+    dlo.dlo_op_linear_noalloc(dlo.DLO_EPI_BIAS, A, W, bias, M, N, K, out)  # first call: one-time set-up
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    dlo.dlo_op_linear_noalloc(dlo.DLO_EPI_BIAS, A, W, bias, M, N, K, out)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+
+
+def test_noalloc_rejects_bad_arguments():
+    A = torch.zeros(16, 16, dtype=torch.int16, device="cuda")
+    with pytest.raises(dlo.DloError) as e:
+        dlo.dlo_op_linear_noalloc(dlo.DLO_EPI_BIAS, A, A, A, 16, 12, 16, A)
+    assert e.value.status == dlo.DLO_ERR_ALIGNMENT
+    with pytest.raises(dlo.DloError) as e:
+        dlo.dlo_op_linear_noalloc(dlo.DLO_EPI_BIAS, A, A, A, 0, 16, 16, A)
+    assert e.value.status == dlo.DLO_ERR_INVALID_ARG
+    with pytest.raises(dlo.DloError) as e:
+        dlo.dlo_op_linear_noalloc(dlo.DLO_EPI_BIAS, A, A, A, 2 ** 31 - 100, 16, 16, A)
+    assert e.value.status == dlo.DLO_ERR_SHAPE
