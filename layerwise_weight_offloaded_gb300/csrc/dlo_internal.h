@@ -33,6 +33,10 @@ int device_info(DeviceInfo* out);
 // 2-D bf16 tensor map over a row-major [rows, inner] matrix with a
 // box of [box_rows, 64] elements and 128-byte swizzle.
 int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
+// 3-D bf16 tensor map over [depth, rows, inner] with a box of [1, box_rows, 64]
+// and 128-byte swizzle (rows past `rows` read as zero within each depth slice).
+int encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
+                        uint32_t box_rows);
 
 // Process-wide device error word for the single-op entry points.
 int op_error_flag(int** flag);
@@ -65,6 +69,7 @@ struct GemmArgs {
 int gemm_block_n(int M, int N, int num_sms);
 int launch_gemm(const CUtensorMap& tmA, const CUtensorMap* tmW, const GemmArgs& a, cudaStream_t st, int num_sms);
 
-int launch_attention(const uint16_t* qkv, int R, int T, int H, int d, uint16_t* o, cudaStream_t st);
+// Non-causal attention on tcgen05; err receives the code of an expired wait.
+int launch_attention(const uint16_t* qkv, int R, int T, int H, int d, uint16_t* o, int* err, cudaStream_t st);
 
 }  // namespace dlo

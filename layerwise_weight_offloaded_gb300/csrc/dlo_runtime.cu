@@ -85,6 +85,23 @@ int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return DLO_OK;
 }
 
+int encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
+                        uint32_t box_rows) {
+    auto enc = tmap_encoder();
+    if (!enc) return set_error(DLO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    if (reinterpret_cast<uintptr_t>(base) % 16 || (inner * 2) % 16)
+        return set_error(DLO_ERR_ALIGNMENT, "tensor map: base or row pitch not 16-byte aligned");
+    cuuint64_t dims[3] = {inner, rows, depth};
+    cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(DLO_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (CUresult %d)", (int)r);
+    return DLO_OK;
+}
+
 int op_error_flag(int** flag) {
     static int* flags[64] = {};
     static std::mutex mu;
@@ -325,7 +342,7 @@ int run_block(dlo_handle* h, int b, float* x, const float* cond, int R, int T, c
     prof_end(e, s);
 
     e = prof_begin(h, DLO_K_ATTENTION, s);
-    if ((rc = launch_attention(h->qkv, R, T, H, d, h->o, s))) return rc;
+    if ((rc = launch_attention(h->qkv, R, T, H, d, h->o, h->d_err, s))) return rc;
     prof_end(e, s);
 
     e = prof_begin(h, DLO_K_GEMM_PROJ, s);
@@ -727,7 +744,9 @@ int dlo_op_attention(const uint16_t* qkv, int32_t R, int32_t T, int32_t H, int32
     if (rc) return rc;
     if (reinterpret_cast<uintptr_t>(qkv) % 16 || reinterpret_cast<uintptr_t>(o) % 16)
         return set_error(DLO_ERR_ALIGNMENT, "attention: qkv and o must be 16-byte aligned");
-    return launch_attention(qkv, R, T, H, d, o, reinterpret_cast<cudaStream_t>(stream));
+    int* err = nullptr;
+    if ((rc = op_error_flag(&err))) return rc;
+    return launch_attention(qkv, R, T, H, d, o, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int dlo_op_shard_gather(const uint16_t* const* shards, int32_t dp, int64_t S, uint16_t* dst, dlo_stream_t stream) {

@@ -216,7 +216,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int m0 = (tile % num_m) * kGemmBM;
             const int n0 = (tile / num_m) * BN;
-            if (!mbar_wait_bounded(&acc_full[acc], acc_phase, p.err, KERR_GEMM_EPILOGUE)) break;
+            // uniform across the warp: the tcgen05.ld below is warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[acc], acc_phase, p.err, KERR_GEMM_EPILOGUE)))
+                break;
             tc_fence_after();
             const int row = m0 + row_in_tile;
             const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);

@@ -192,6 +192,42 @@ def test_attention_vs_oracle(R, T, H, d):
         assert np.all(err <= BF16_REL * np.abs(ref) + 8e-3 * np.abs(ref).max()), err.max()
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_attention_growing_logits_vs_oracle(d):
+    """Keys whose logits grow along the sequence raise the running max many
+    times (the rescaling path of the online softmax)."""
+    R, T, H = 1, 1000, 2
+    h = H * d
+    vals = synthetic.normal_f32(9, d, (T, 3 * h), 1.0)
+    vals[:, h:2 * h] *= (1.0 + 6.0 * np.arange(T) / T).astype(np.float32)[:, None]
+    qkv = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).cuda()
+    o = torch.empty(T, h, dtype=torch.int16, device="cuda")
+    dlo.dlo_op_attention(qkv, R, T, H, d, o)
+    dlo.dlo_op_check()
+    q = bf16_bits_to_f64(to_bits(qkv)).reshape(T, 3 * h)
+    ref = dit.attention(q[:, :h], q[:, h:2 * h], q[:, 2 * h:], H)
+    got = bf16_bits_to_f64(to_bits(o)).reshape(T, h)
+    err = np.abs(got - ref)
+    assert np.all(err <= BF16_REL * np.abs(ref) + 8e-3 * np.abs(ref).max()), err.max()
+
+
+@pytest.mark.parametrize("R,T,H,d", [(1, 4096, 2, 64), (2, 16384, 1, 128)])
+def test_attention_long_sequences_sampled_rows(R, T, H, d):
+    """Workload-length sequences: sampled query rows against the oracle."""
+    h = H * d
+    qkv, qb = bf16_tensor(10, T, (R * T, 3 * h), 1.0)
+    o = torch.empty(R * T, h, dtype=torch.int16, device="cuda")
+    dlo.dlo_op_attention(qkv, R, T, H, d, o)
+    dlo.dlo_op_check()
+    q = bf16_bits_to_f64(qb).reshape(R, T, 3 * h)
+    got = bf16_bits_to_f64(to_bits(o)).reshape(R, T, h)
+    rows = np.array([0, 1, 127, 128, T // 2, T - 129, T - 1])
+    for r in range(R):
+        ref = dit.attention(q[r, rows, :h], q[r, :, h:2 * h], q[r, :, 2 * h:], H)
+        err = np.abs(got[r, rows] - ref)
+        assert np.all(err <= BF16_REL * np.abs(ref) + 8e-3 * np.abs(ref).max()), err.max()
+
+
 def test_attention_single_token_returns_v():
     """Closed form: one key gets softmax weight exactly 1, so O = V bit for bit."""
     R, T, H, d = 3, 1, 4, 64
