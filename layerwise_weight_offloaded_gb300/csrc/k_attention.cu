@@ -6,28 +6,33 @@
 // O = softmax(Q K^T / sqrt(d)) V: fp32 logits in TMEM, fp32 online softmax,
 // softmax weights rounded to bf16 for the P.V product, fp32 accumulation.
 //
-// One CTA = 128 query rows of one (request, head), 6 warps:
-//   warp 0     TMA producer: Q once, then 128-key K and V tiles into a
-//              STAGES-deep ring (3-D tensor map over [R, T, 3h], so a tile
-//              never reaches into the next request: rows past T read zero);
-//   warp 1     allocates TMEM (two 128-column S buffers + d columns of O);
-//              lane 0 issues S_j = Q K_j^T (both operands K-major) into S
-//              buffer j%2 and O += P_j V_j (P K-major from shared memory, V
-//              MN-major straight from its TMA tile);
-//   warps 2-5  softmax, one query row per thread (warp w owns TMEM lanes
-//              32*(w%4)..+31): tcgen05.ld of the S row, keys past T masked to
-//              -inf, running max m and sum l, P = exp2(S*c - m) written to
-//              shared memory in the 128-byte-swizzled K-major layout the MMA
-//              reads.  The running max is raised lazily - only when a row's
-//              max grows by more than 2^8 - and O in TMEM is rescaled then;
-//              otherwise P may reach 2^8, which fp32 and bf16 represent with
-//              their usual relative precision, and O / l is the same softmax.
-//              Finally O / l is written out as bf16.
-// S is double-buffered so the next QK^T runs while this tile's softmax does.
-// tcgen05.ld/st are warp-collective, so every branch around them is made
-// uniform across the warp (__any_sync / __all_sync).  Every wait is bounded;
-// on expiry the CTA records a code, drains its own copies and MMAs, frees
-// TMEM and returns.
+// One CTA = two 128-row query tiles of one (request, head), 10 warps:
+//   warp 0     TMA producer: both Q tiles once, then 128-key K and V tiles into
+//              a STAGES-deep ring shared by the two query tiles (3-D tensor map
+//              over [R, T, 3h]: a tile never reaches into the next request,
+//              rows past T read zero);
+//   warp 1     allocates all 512 TMEM columns; lane 0 issues, per key tile j
+//              and query tile t, S(t,j) = Q_t K_j^T (both operands K-major
+//              from shared memory) and O_t += P(t,j) V_j with P read from TMEM
+//              and V MN-major straight from its TMA tile;
+//   warps 2-5  softmax of query tile 0, warps 6-9 of query tile 1: one query
+//              row per thread (warp w owns TMEM lanes 32*(w%4)..+31).  Each
+//              tcgen05.ld's the S row, masks keys past T, keeps the running
+//              max m and sum l, and writes P = 2^(S*c - m) as packed bf16 back
+//              into TMEM with tcgen05.st.  The max is raised lazily - only
+//              when a row's max grows by more than 2^8 - and O in TMEM is
+//              rescaled then; otherwise P may reach 2^8 and O / l is the same
+//              softmax.  At the end each thread writes its row of O / l.
+// The tensor core alternates between the two query tiles, so one tile's
+// MMAs run while the other tile's softmax does.
+//   d = 64 : TMEM per tile [S 128 | P 64 | O 64]; the softmax frees S as soon
+//            as it has loaded it, so S(t,j+1) can start during softmax(t,j).
+//   d = 128: TMEM per tile S 128 with P written over its first 64 columns,
+//            O 128 elsewhere; S(t,j+1) is issued after P(t,j) has been read.
+// tcgen05.ld/st are warp-collective, so every branch around them is uniform
+// across the warp (__any_sync / __all_sync).  Every wait is bounded; on
+// expiry the CTA records a code, drains its own copies and MMAs, frees TMEM
+// and returns.
 #include "dlo_device.cuh"
 #include "dlo_internal.h"
 
@@ -35,23 +40,26 @@ namespace dlo {
 
 namespace {
 
-constexpr int kAttBM = 128;   // query rows per CTA
+constexpr int kAttBM = 128;   // query rows per tile (two tiles per CTA)
 constexpr int kAttBN = 128;   // keys per tile
-constexpr int kAttThreads = 192;
+constexpr int kAttThreads = 320;
 constexpr int kTileBytes = 128 * 128;  // one 128-row x 64-col bf16 box = 16 KB
 constexpr float kLazyRescale = 8.0f;   // log2 units
 
 template <int D>
 struct AttCfg {
+    static constexpr bool kAliasP = D == 128;              // P over the first half of S
     static constexpr int kChunks = D / 64;                  // 64-wide column chunks of a head
-    static constexpr int kQBytes = kChunks * kTileBytes;    // Q tile
+    static constexpr int kQBytes = kChunks * kTileBytes;    // one Q tile
     static constexpr int kKVBytes = kChunks * kTileBytes;   // one K (or V) tile
-    static constexpr int kPBytes = 2 * kTileBytes;          // 128 x 128 bf16 P tile
-    static constexpr int kStages = D == 64 ? 3 : 2;
-    static constexpr int kSmem = kQBytes + 2 * kStages * kKVBytes + 2 * kPBytes;
+    static constexpr int kStages = D == 64 ? 4 : 2;
+    static constexpr int kSmem = 2 * kQBytes + 2 * kStages * kKVBytes;
     static constexpr int kSmemAlloc = kSmem + 1024 + 256;
-    static constexpr uint32_t kTmemCols = 512;              // S0 | S1 | O
-    static constexpr uint32_t kOCol = 256;
+    static constexpr uint32_t kTmemCols = 512;
+    // column offsets of tile t's regions
+    __host__ __device__ static constexpr uint32_t s_col(int t) { return kAliasP ? t * 128 : t * 256; }
+    __host__ __device__ static constexpr uint32_t p_col(int t) { return kAliasP ? t * 128 : t * 256 + 128; }
+    __host__ __device__ static constexpr uint32_t o_col(int t) { return kAliasP ? 256 + t * 128 : t * 256 + 192; }
 };
 
 }  // namespace
@@ -71,24 +79,24 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     constexpr int ST = Cfg::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem;
-    uint8_t* sK = sQ + Cfg::kQBytes;               // stage s at sK + s*kKVBytes
+    uint8_t* sQ = smem;                            // tile t at sQ + t*kQBytes
+    uint8_t* sK = sQ + 2 * Cfg::kQBytes;           // stage s at sK + s*kKVBytes
     uint8_t* sV = sK + ST * Cfg::kKVBytes;
-    uint8_t* sP = sV + ST * Cfg::kKVBytes;         // buffer b at sP + b*kPBytes
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Cfg::kSmem);
     uint64_t* q_full = bar;
     uint64_t* k_full = bar + 1;
     uint64_t* k_empty = k_full + ST;
     uint64_t* v_full = k_empty + ST;
     uint64_t* v_empty = v_full + ST;
-    uint64_t* s_full = v_empty + ST;   // [2]
-    uint64_t* p_full = s_full + 2;     // [2]
+    uint64_t* s_full = v_empty + ST;   // [2] per query tile
+    uint64_t* s_free = s_full + 2;     // [2]
+    uint64_t* p_full = s_free + 2;     // [2]
     uint64_t* o_done = p_full + 2;     // [2]
     uint64_t* drain = o_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int q0 = blockIdx.x * kAttBM;
+    const int q0 = blockIdx.x * 2 * kAttBM;
     const int head = blockIdx.y;
     const int req = blockIdx.z;
     const int h = H * D;
@@ -102,10 +110,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], 128);
-            mbar_init(&o_done[b], 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&s_free[t], 128);
+            mbar_init(&p_full[t], 128);
+            mbar_init(&o_done[t], 1);
         }
         mbar_init(drain, 1);
         fence_mbarrier_init();
@@ -121,9 +130,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         if (lane == 0) {
             // ---------------- TMA producer
             long issued_k = 0, issued_v = 0;
-            mbar_arrive_expect_tx(q_full, Cfg::kQBytes);
-            for (int c = 0; c < Cfg::kChunks; ++c)
-                tma_load_3d(sQ + c * kTileBytes, &tm, head * D + c * 64, q0, req, q_full);
+            mbar_arrive_expect_tx(q_full, 2 * Cfg::kQBytes);
+            for (int t = 0; t < 2; ++t)
+                for (int c = 0; c < Cfg::kChunks; ++c)
+                    tma_load_3d(sQ + t * Cfg::kQBytes + c * kTileBytes, &tm, head * D + c * 64, q0 + t * kAttBM, req,
+                                q_full);
             for (int j = 0; j < n_kv; ++j) {
                 const int s = j % ST;
                 const uint32_t ph = (uint32_t)((j / ST) & 1);
@@ -152,148 +163,176 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             // ---------------- MMA issuer
             constexpr uint32_t idesc_s = umma_idesc_bf16_f32(kAttBM, kAttBN);
             constexpr uint32_t idesc_pv = umma_idesc_bf16_f32(kAttBM, D) | (1u << 16);  // B (= V) MN-major
-            const uint32_t q_addr = smem_u32(sQ);
-            bool ok = mbar_wait_bounded(q_full, 0, err, KERR_ATT_MMA);
-            auto issue_s = [&](int j) -> bool {
-                const int s = j % ST;
-                if (!mbar_wait_bounded(&k_full[s], (uint32_t)((j / ST) & 1), err, KERR_ATT_MMA)) return false;
-                tc_fence_after();
-                const uint32_t k_addr = smem_u32(sK + s * Cfg::kKVBytes);
-                const uint32_t d_tmem = tmem + (uint32_t)((j & 1) * kAttBN);
+            // S(t, j) = Q_t K_j^T into tile t's S columns
+            auto issue_s = [&](int t, int j) {
+                const uint32_t q_addr = smem_u32(sQ + t * Cfg::kQBytes);
+                const uint32_t k_addr = smem_u32(sK + (j % ST) * Cfg::kKVBytes);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (uint32_t)((kk >> 2) * kTileBytes + (kk & 3) * 32);
-                    umma_bf16(d_tmem, umma_desc_sw128(q_addr + off), umma_desc_sw128(k_addr + off), idesc_s, kk > 0);
+                    umma_bf16(tmem + Cfg::s_col(t), umma_desc_sw128(q_addr + off), umma_desc_sw128(k_addr + off),
+                              idesc_s, kk > 0);
                 }
-                umma_commit(&k_empty[s]);
-                umma_commit(&s_full[j & 1]);
-                return true;
+                umma_commit(&s_full[t]);
             };
-            if (ok) ok = issue_s(0);
-            if (ok && n_kv > 1) ok = issue_s(1);
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int b = j & 1;
-                if (!mbar_wait_bounded(&p_full[b], (uint32_t)((j >> 1) & 1), err, KERR_ATT_MMA)) break;
-                const int s = j % ST;
-                if (!mbar_wait_bounded(&v_full[s], (uint32_t)((j / ST) & 1), err, KERR_ATT_MMA)) break;
-                tc_fence_after();
-                const uint32_t p_addr = smem_u32(sP + b * Cfg::kPBytes);
-                const uint32_t v_addr = smem_u32(sV + s * Cfg::kKVBytes);
+            // O_t += P(t, j) V_j, P from TMEM (16 keys = 8 packed columns per step)
+            auto issue_pv = [&](int t, int j) {
+                const uint32_t v_addr = smem_u32(sV + (j % ST) * Cfg::kKVBytes);
 #pragma unroll
-                for (int kk = 0; kk < kAttBN / 16; ++kk) {
-                    const uint32_t poff = (uint32_t)((kk >> 2) * kTileBytes + (kk & 3) * 32);
-                    umma_bf16(tmem + Cfg::kOCol, umma_desc_sw128(p_addr + poff),
-                              umma_desc_sw128_mn(v_addr + (uint32_t)(kk * 2048), kTileBytes), idesc_pv,
-                              (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kAttBN / 16; ++kk)
+                    umma_bf16_ts(tmem + Cfg::o_col(t), tmem + Cfg::p_col(t) + (uint32_t)(kk * 8),
+                                 umma_desc_sw128_mn(v_addr + (uint32_t)(kk * 2048), kTileBytes), idesc_pv,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&o_done[t]);
+            };
+            bool ok = mbar_wait_bounded(q_full, 0, err, KERR_ATT_MMA) &&
+                      mbar_wait_bounded(&k_full[0], 0, err, KERR_ATT_MMA);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                issue_s(1, 0);
+                umma_commit(&k_empty[0]);
+            }
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const uint32_t ph = (uint32_t)(j & 1);
+                const bool next = j + 1 < n_kv;
+                const int sn = (j + 1) % ST;
+                if (next && !(ok = mbar_wait_bounded(&k_full[sn], (uint32_t)(((j + 1) / ST) & 1), err, KERR_ATT_MMA)))
+                    break;
+                if (!(ok = mbar_wait_bounded(&v_full[j % ST], (uint32_t)((j / ST) & 1), err, KERR_ATT_MMA))) break;
+                if constexpr (!Cfg::kAliasP) {
+                    // S(t, j+1) as soon as softmax(t, j) has loaded S(t, j); then the P.V products
+                    if (next) {
+                        for (int t = 0; t < 2 && ok; ++t) {
+                            if (!(ok = mbar_wait_bounded(&s_free[t], ph, err, KERR_ATT_MMA))) break;
+                            tc_fence_after();
+                            issue_s(t, j + 1);
+                        }
+                        if (!ok) break;
+                        umma_commit(&k_empty[sn]);
+                    }
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (!(ok = mbar_wait_bounded(&p_full[t], ph, err, KERR_ATT_MMA))) break;
+                        tc_fence_after();
+                        issue_pv(t, j);
+                    }
+                } else {
+                    // P lives in S's columns: S(t, j+1) is issued only once PV(t, j),
+                    // which reads P there, has completed.  Both PVs are queued first so
+                    // the tensor core stays busy while this thread waits.
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (!(ok = mbar_wait_bounded(&p_full[t], ph, err, KERR_ATT_MMA))) break;
+                        tc_fence_after();
+                        issue_pv(t, j);
+                    }
+                    if (ok && next) {
+                        for (int t = 0; t < 2 && ok; ++t) {
+                            if (!(ok = mbar_wait_bounded(&o_done[t], ph, err, KERR_ATT_MMA))) break;
+                            tc_fence_after();
+                            issue_s(t, j + 1);
+                        }
+                        if (ok) umma_commit(&k_empty[sn]);
+                    }
                 }
-                umma_commit(&v_empty[s]);
-                umma_commit(&o_done[b]);
-                if (j + 2 < n_kv) ok = issue_s(j + 2);
+                if (ok) umma_commit(&v_empty[j % ST]);
             }
             umma_commit(drain);
             mbar_wait_bounded(drain, 0, err, KERR_ATT_DRAIN);
         }
     } else {
-        // ---------------- softmax warpgroup (warps 2..5); all control flow
-        // that encloses a tcgen05.ld/st is uniform across the warp.
+        // ---------------- softmax warpgroups: warps 2-5 tile 0, warps 6-9 tile 1.
+        // All control flow around tcgen05.ld/st is uniform across the warp.
+        const int t = warp >= 6 ? 1 : 0;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const uint32_t s_addr = tmem + lane_base + Cfg::s_col(t);
+        const uint32_t p_addr = tmem + lane_base + Cfg::p_col(t);
+        const uint32_t o_addr = tmem + lane_base + Cfg::o_col(t);
         const unsigned FULL = 0xffffffffu;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            const int b = j & 1;
-            ok = __all_sync(FULL, mbar_wait_bounded(&s_full[b], (uint32_t)((j >> 1) & 1), err, KERR_ATT_SOFTMAX));
+            const uint32_t ph = (uint32_t)(j & 1);
+            ok = __all_sync(FULL, mbar_wait_bounded(&s_full[t], ph, err, KERR_ATT_SOFTMAX));
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[kAttBN];
+            float s[kAttBN];
 #pragma unroll
             for (int c = 0; c < kAttBN / 32; ++c)
-                tmem_ld_32x32b_x32_nowait(tmem + lane_base + (uint32_t)(b * kAttBN + c * 32), sr + c * 32);
+                tmem_ld_32x32b_x32_nowait(s_addr + (uint32_t)(c * 32), reinterpret_cast<uint32_t*>(s) + c * 32);
             tmem_ld_wait();
-            float t[kAttBN];
-            const int valid = T - j * kAttBN;  // keys of this tile that exist
-            float mx = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < kAttBN; ++i) {
-                t[i] = (i < valid) ? __uint_as_float(sr[i]) * scale_log2 : -INFINITY;
-                mx = fmaxf(mx, t[i]);
+            if constexpr (!Cfg::kAliasP) {
+                tc_fence_before();
+                mbar_arrive(&s_free[t]);  // S(t, j+1) may now be written
             }
-            if (j == 0) {
-                m = mx;
-            } else {
-                // Raise this row's running max only if it grew by more than 2^8.
+            const int valid = T - j * kAttBN;  // keys of this tile that exist (uniform)
+            if (valid < kAttBN) {
+#pragma unroll
+                for (int i = 0; i < kAttBN; ++i)
+                    if (i >= valid) s[i] = -INFINITY;
+            }
+            float mx4[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+            for (int i = 4; i < kAttBN; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+            if (j > 0) {
+                // PV(t, j-1) must have landed before O is rescaled or P overwritten
+                ok = __all_sync(FULL, mbar_wait_bounded(&o_done[t], ph ^ 1u, err, KERR_ATT_SOFTMAX));
+                if (!ok) break;
+                tc_fence_after();
                 const bool raise = mx > m + kLazyRescale;
                 if (__any_sync(FULL, raise)) {
-                    // The whole warp rescales its O rows (alpha = 1 for rows that keep
-                    // their max) once PV_{j-1} has landed in TMEM.
-                    const float alpha = raise ? exp2f(m - mx) : 1.0f;
+                    const float alpha = raise ? ex2_approx(m - mx) : 1.0f;
                     if (raise) {
                         m = mx;
                         l *= alpha;
                     }
-                    const int pb = (j - 1) & 1;
-                    ok = __all_sync(FULL, mbar_wait_bounded(&o_done[pb], (uint32_t)(((j - 1) >> 1) & 1), err,
-                                                            KERR_ATT_SOFTMAX));
-                    if (!ok) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t orow[32];
-                        const uint32_t oaddr = tmem + lane_base + Cfg::kOCol + (uint32_t)(c * 32);
-                        tmem_ld_32x32b_x32_nowait(oaddr, orow);
+#pragma unroll 1
+                    for (int c = 0; c < D / 16; ++c) {
+                        uint32_t orow[16];
+                        tmem_ld_32x32b_x16_nowait(o_addr + (uint32_t)(c * 16), orow);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
-                        tmem_st_32x32b_x32(oaddr, orow);
+                        for (int i = 0; i < 16; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+                        tmem_st_32x32b_x16(o_addr + (uint32_t)(c * 16), orow);
                     }
-                    tmem_st_wait();
                 }
+            } else {
+                m = mx;
             }
-            // P buffer b was last read by PV_{j-2}
-            if (j >= 2) {
-                ok = __all_sync(FULL, mbar_wait_bounded(&o_done[b], (uint32_t)(((j - 2) >> 1) & 1), err,
-                                                        KERR_ATT_SOFTMAX));
-                if (!ok) break;
-            }
-            float rs = 0.f;
-            uint8_t* prow = sP + b * Cfg::kPBytes + (row >> 3) * 1024 + (row & 7) * 128;
+            const float neg_m = -m;
+            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int q = 0; q < 4; ++q) {  // 32 keys -> 16 packed columns per store
+                uint32_t pk[16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    float p[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        p[e] = exp2f(t[c * 64 + u * 8 + e] - m);
-                        rs += p[e];
-                    }
-                    uint4 w;
-                    w.x = pack_bf16x2(p[0], p[1]);
-                    w.y = pack_bf16x2(p[2], p[3]);
-                    w.z = pack_bf16x2(p[4], p[5]);
-                    w.w = pack_bf16x2(p[6], p[7]);
-                    *reinterpret_cast<uint4*>(prow + c * kTileBytes + ((u ^ (row & 7)) << 4)) = w;
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = ex2_approx(fmaf(s[q * 32 + 2 * i], scale_log2, neg_m));
+                    const float p1 = ex2_approx(fmaf(s[q * 32 + 2 * i + 1], scale_log2, neg_m));
+                    rs4[(2 * i) & 3] += p0;
+                    rs4[(2 * i + 1) & 3] += p1;
+                    pk[i] = pack_bf16x2(p0, p1);
                 }
+                tmem_st_32x32b_x16(p_addr + (uint32_t)(q * 16), pk);
             }
-            l += rs;
-            fence_proxy_async_smem();
+            l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+            tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&p_full[b]);
+            mbar_arrive(&p_full[t]);
         }
-        // O / l for this row, after the last P.V product
-        if (ok) ok = __all_sync(FULL, mbar_wait_bounded(&o_done[(n_kv - 1) & 1], (uint32_t)(((n_kv - 1) >> 1) & 1),
-                                                        err, KERR_ATT_SOFTMAX));
+        // O / l for this row, after the last P.V product of this tile
+        if (ok) ok = __all_sync(FULL, mbar_wait_bounded(&o_done[t], (uint32_t)((n_kv - 1) & 1), err,
+                                                        KERR_ATT_SOFTMAX));
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
-            const int t_row = q0 + row;
+            const int t_row = q0 + t * kAttBM + row;
             uint16_t* orow = o + ((size_t)req * T + t_row) * h + head * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
-                tmem_ld_32x32b_x32_nowait(tmem + lane_base + Cfg::kOCol + (uint32_t)(c * 32), v);
+                tmem_ld_32x32b_x32_nowait(o_addr + (uint32_t)(c * 32), v);
                 tmem_ld_wait();
                 if (t_row < T) {
 #pragma unroll
@@ -335,7 +374,7 @@ static int launch_attention_t(const uint16_t* qkv, int R, int T, int H, uint16_t
     int rc = encode_tmap_bf16_3d(&tm, qkv, 3 * h, (uint64_t)T, (uint64_t)R, 128);
     if (rc) return rc;
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-    dim3 grid((T + kAttBM - 1) / kAttBM, H, R);
+    dim3 grid((T + 2 * kAttBM - 1) / (2 * kAttBM), H, R);
     attention_fwd_tcgen05<D><<<grid, kAttThreads, Cfg::kSmemAlloc, st>>>(tm, T, H, o, scale_log2, err);
     DLO_CUDA_TRY(cudaGetLastError());
     return DLO_OK;
