@@ -224,6 +224,8 @@ def main():
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")  # > 129 MB L2
 
+    clocks = ClockSampler(dev)
+    clocks.start()  # started before the warm-up so its start-up cost never lands in a timed step
     for _ in range(args.warmup):
         x.copy_(x0)
         dlo.dlo_forward(h, x, cond, R, T, stream)
@@ -234,12 +236,10 @@ def main():
     ktime = {k: 0.0 for k in kclasses}
     klaunch = {k: 0 for k in kclasses}
     launches0 = dlo.dlo_get_stats(h)["kernel_launches"]
-    clocks = ClockSampler(dev)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    total_ms = 0.0
+    step_ms = []
     for _ in range(args.steps):
         x.copy_(x0)
         flush.fill_(1)  # evict L2 between steps (outside the timed events)
@@ -249,7 +249,7 @@ def main():
         dlo.dlo_forward(h, x, cond, R, T, stream)
         b.record(stream)
         b.synchronize()
-        total_ms += a.elapsed_time(b)
+        step_ms.append(a.elapsed_time(b))
         if profile:
             for k, (ms, n) in dlo.dlo_get_kernel_times(h).items():
                 ktime[k] += ms
@@ -258,7 +258,7 @@ def main():
     clk = clocks.stop()
     dlo.dlo_synchronize(h, 600000)
     launches = dlo.dlo_get_stats(h)["kernel_launches"] - launches0
-    ms_step = total_ms / args.steps
+    ms_step = sum(step_ms) / args.steps
     if dist:
         t = torch.tensor([ms_step], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -324,6 +324,7 @@ def main():
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
                    "l2": "flushed between steps (256 MB write)", "fill": args.fill},
         "block_forwards_per_s": L * world / (ms_step * 1e-3),
+        "step_ms": {"min": min(step_ms), "median": float(np.median(step_ms)), "max": max(step_ms)},
         "path_roofline": {"frac": path_frac, "per_block_roofline_ms": roof_block_s * 1e3,
                           "bound": "host-link" if block_bytes / bw > (gemm_f + attn_f + ada_f) / p_tc else "tensor",
                           "h2d_gbs_measured": bw / 1e9, "block_bytes": block_bytes,

@@ -22,7 +22,10 @@
 //              into TMEM with tcgen05.st.  The max is raised lazily - only
 //              when a row's max grows by more than 2^8 - and O in TMEM is
 //              rescaled then; otherwise P may reach 2^8 and O / l is the same
-//              softmax.  At the end each thread writes its row of O / l.
+//              softmax.  Scale-and-subtract and the row sum use packed fp32x2
+//              instructions and the max a 3-input max, so a thread spends about
+//              three instructions per logit besides the exponential.  At the
+//              end each thread writes its row of O / l.
 // The tensor core alternates between the two query tiles, so one tile's
 // MMAs run while the other tile's softmax does.
 //   d = 64 : TMEM per tile [S 128 | P 64 | O 64]; the softmax frees S as soon
@@ -45,6 +48,31 @@ constexpr int kAttBN = 128;   // keys per tile
 constexpr int kAttThreads = 320;
 constexpr int kTileBytes = 128 * 128;  // one 128-row x 64-col bf16 box = 16 KB
 constexpr float kLazyRescale = 8.0f;   // log2 units
+
+// Packed fp32x2 arithmetic (sm_100+): two independent fp32 lanes per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 template <int D>
 struct AttCfg {
@@ -201,21 +229,20 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     break;
                 if (!(ok = mbar_wait_bounded(&v_full[j % ST], (uint32_t)((j / ST) & 1), err, KERR_ATT_MMA))) break;
                 if constexpr (!Cfg::kAliasP) {
-                    // S(t, j+1) as soon as softmax(t, j) has loaded S(t, j); then the P.V products
-                    if (next) {
-                        for (int t = 0; t < 2 && ok; ++t) {
+                    // per query tile: S(t, j+1) once softmax(t, j) has loaded S(t, j),
+                    // then PV(t, j) once it has written P; the two tiles do not wait
+                    // on each other
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (next) {
                             if (!(ok = mbar_wait_bounded(&s_free[t], ph, err, KERR_ATT_MMA))) break;
                             tc_fence_after();
                             issue_s(t, j + 1);
                         }
-                        if (!ok) break;
-                        umma_commit(&k_empty[sn]);
-                    }
-                    for (int t = 0; t < 2 && ok; ++t) {
                         if (!(ok = mbar_wait_bounded(&p_full[t], ph, err, KERR_ATT_MMA))) break;
                         tc_fence_after();
                         issue_pv(t, j);
                     }
+                    if (ok && next) umma_commit(&k_empty[sn]);
                 } else {
                     // P lives in S's columns: S(t, j+1) is issued only once PV(t, j),
                     // which reads P there, has completed.  Both PVs are queued first so
@@ -272,10 +299,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 for (int i = 0; i < kAttBN; ++i)
                     if (i >= valid) s[i] = -INFINITY;
             }
-            float mx4[4] = {s[0], s[1], s[2], s[3]};
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 4; i < kAttBN; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+            for (int i = 0; i < kAttBN / 2; ++i) mx4[i & 3] = max3f(mx4[i & 3], s[2 * i], s[2 * i + 1]);
+            const float mx = max3f(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * scale_log2;
             if (j > 0) {
                 // PV(t, j-1) must have landed before O is rescaled or P overwritten
                 ok = __all_sync(FULL, mbar_wait_bounded(&o_done[t], ph ^ 1u, err, KERR_ATT_SOFTMAX));
@@ -301,21 +328,26 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             } else {
                 m = mx;
             }
-            const float neg_m = -m;
-            float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint64_t c2 = f2_pack(scale_log2, scale_log2);
+            const uint64_t nm2 = f2_pack(-m, -m);
+            uint64_t acc2[2] = {0ull, 0ull};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {  // 32 keys -> 16 packed columns per store
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const float p0 = ex2_approx(fmaf(s[q * 32 + 2 * i], scale_log2, neg_m));
-                    const float p1 = ex2_approx(fmaf(s[q * 32 + 2 * i + 1], scale_log2, neg_m));
-                    rs4[(2 * i) & 3] += p0;
-                    rs4[(2 * i + 1) & 3] += p1;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(s[q * 32 + 2 * i], s[q * 32 + 2 * i + 1]), c2, nm2), x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    acc2[i & 1] = f2_add(acc2[i & 1], f2_pack(p0, p1));
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 tmem_st_32x32b_x16(p_addr + (uint32_t)(q * 16), pk);
             }
+            float a0, a1, b0, b1;
+            f2_unpack(acc2[0], a0, a1);
+            f2_unpack(acc2[1], b0, b1);
+            float rs4[4] = {a0, a1, b0, b1};
             l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
             tmem_st_wait();
             tc_fence_before();
