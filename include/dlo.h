@@ -121,7 +121,7 @@ typedef struct {
 
 /* Kernel classes reported by dlo_get_kernel_times. */
 enum {
-    DLO_K_FILL = 0,      /* zero-copy shard gather (0 when the copy engine fills) */
+    DLO_K_FILL = 0,      /* slot fill on the copy stream (copy-engine copies or the gather kernel) */
     DLO_K_ADALN = 1,     /* modulation GEMV */
     DLO_K_LN_MOD = 2,    /* LayerNorm + modulate (twice per block) */
     DLO_K_GEMM_QKV = 3,
@@ -129,7 +129,8 @@ enum {
     DLO_K_GEMM_PROJ = 5,
     DLO_K_GEMM_FC1 = 6,
     DLO_K_GEMM_FC2 = 7,
-    DLO_K_NUM = 8
+    DLO_K_FILL_WAIT = 8, /* compute stream blocked on a slot that is not filled yet */
+    DLO_K_NUM = 9
 };
 
 /* ---------------- host-only helpers (no GPU needed) ---------------- */
@@ -212,8 +213,8 @@ int dlo_synchronize(dlo_handle* h, int32_t timeout_ms);
 
 int dlo_get_stats(dlo_handle* h, dlo_stats* out);
 
-/* With DLO_PROFILE: per kernel class (DLO_K_*), total device milliseconds and
- * launches of the most recent dlo_forward.  Synchronises with that forward.
+/* With DLO_PROFILE: per class (DLO_K_*), total device milliseconds and
+ * launches (or occurrences) of the most recent dlo_forward.  Synchronises with that forward.
  * Both arrays hold DLO_K_NUM entries. */
 int dlo_get_kernel_times(dlo_handle* h, double* ms, int64_t* launches);
 

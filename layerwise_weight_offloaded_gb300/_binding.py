@@ -33,7 +33,8 @@ DLO_EPI_BIAS = 0
 DLO_EPI_BIAS_GELU = 1
 DLO_EPI_GATED_RESIDUAL = 2
 
-KERNEL_CLASSES = ("fill", "adaln", "ln_modulate", "gemm_qkv", "attention", "gemm_proj", "gemm_fc1", "gemm_fc2")
+KERNEL_CLASSES = ("fill", "adaln", "ln_modulate", "gemm_qkv", "attention", "gemm_proj", "gemm_fc1", "gemm_fc2",
+                  "fill_wait")
 DLO_K_NUM = len(KERNEL_CLASSES)
 
 # Every symbol include/dlo.h declares (checked by the CPU test suite).

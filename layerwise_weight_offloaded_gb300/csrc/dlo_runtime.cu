@@ -568,7 +568,7 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
         // Slots may still be read by earlier work on `s`: the first fill waits for it.
         FWD_TRY(cudaEventRecord(h->start_ev, s));
         FWD_TRY(cudaStreamWaitEvent(h->copy, h->start_ev, 0));
-        ProfEvent* pe = h->fill_mode == DLO_FILL_ZEROCOPY ? prof_begin(h, DLO_K_FILL, h->copy) : nullptr;
+        ProfEvent* pe = prof_begin(h, DLO_K_FILL, h->copy);
         if ((rc = issue_fill(h, 0, h->slot[0], h->fill_mode))) return fail(h, rc);
         prof_end(pe, h->copy);
         FWD_TRY(cudaEventRecord(h->filled[0], h->copy));
@@ -579,12 +579,14 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
             if (N + 1 < h->L) {
                 const int ns = (N + 1) & 1;
                 if (N + 1 >= 2) FWD_TRY(cudaStreamWaitEvent(h->copy, h->freed[ns], 0));
-                ProfEvent* pe = h->fill_mode == DLO_FILL_ZEROCOPY ? prof_begin(h, DLO_K_FILL, h->copy) : nullptr;
+                ProfEvent* pe = prof_begin(h, DLO_K_FILL, h->copy);
                 if ((rc = issue_fill(h, N + 1, h->slot[ns], h->fill_mode))) return fail(h, rc);
                 prof_end(pe, h->copy);
                 FWD_TRY(cudaEventRecord(h->filled[ns], h->copy));
             }
+            ProfEvent* pw = prof_begin(h, DLO_K_FILL_WAIT, s);
             FWD_TRY(cudaStreamWaitEvent(s, h->filled[slot], 0));
+            prof_end(pw, s);
         }
         if ((rc = run_block(h, N, x, cond, R, T, s))) return fail(h, rc);
         if (!h->resident) FWD_TRY(cudaEventRecord(h->freed[slot], s));

@@ -77,16 +77,20 @@ int launch_shard_gather(const uint16_t* const* shards, int dp, int64_t S, uint16
 // ------------------------------------------------------------------ adaLN modulation
 
 constexpr int kAdaMaxC = 1024;
-constexpr int kAdaRChunk = 4;
+constexpr int kAdaRChunk = 4;     // requests per pass over the weights
+constexpr int kAdaRowsPerWarp = 4; // output features per warp, loads issued together
 
-// One warp per output feature n: mod[r, n] = sum_c ada_w[n, c] * SiLU(cond[r, c]) + ada_b[n].
-// SiLU(cond) for up to kAdaRChunk requests is staged in shared memory.
+// mod[r, n] = sum_c ada_w[n, c] * SiLU(cond[r, c]) + ada_b[n].  SiLU(cond) for up
+// to kAdaRChunk requests is staged in shared memory; each warp owns
+// kAdaRowsPerWarp consecutive features and issues all their 16-byte weight
+// loads before the dot products, so a warp keeps several loads in flight.
 __global__ void __launch_bounds__(256) adaln_gemv(const uint16_t* __restrict__ W, const uint16_t* __restrict__ b,
                                                   const float* __restrict__ cond, int R, int C, int N,
                                                   float* __restrict__ mod) {
-    __shared__ float sc[kAdaRChunk * kAdaMaxC];  // SiLU(cond) of up to kAdaRChunk requests
+    __shared__ float sc[kAdaRChunk * kAdaMaxC];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n = blockIdx.x * 8 + warp;
+    const int n0 = (blockIdx.x * 8 + warp) * kAdaRowsPerWarp;
+    const int steps = (C + 255) / 256;  // 8 weights per lane per step
     for (int r0 = 0; r0 < R; r0 += kAdaRChunk) {
         const int rc = min(kAdaRChunk, R - r0);
         __syncthreads();
@@ -95,29 +99,40 @@ __global__ void __launch_bounds__(256) adaln_gemv(const uint16_t* __restrict__ W
             sc[i] = c / (1.0f + expf(-c));
         }
         __syncthreads();
-        if (n < N) {
-            float acc[kAdaRChunk] = {0.f, 0.f, 0.f, 0.f};
-            const uint16_t* wrow = W + (size_t)n * C;
-            for (int c0 = lane * 8; c0 < C; c0 += 256) {
-                const uint4 w = __ldg(reinterpret_cast<const uint4*>(wrow + c0));
-                const float wf[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
-                                     bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+        float acc[kAdaRowsPerWarp][kAdaRChunk] = {};
+        for (int st = 0; st < steps; ++st) {
+            const int c0 = st * 256 + lane * 8;
+            uint4 w[kAdaRowsPerWarp];
 #pragma unroll
-                for (int r = 0; r < kAdaRChunk; ++r) {
-                    if (r < rc) {
+            for (int k = 0; k < kAdaRowsPerWarp; ++k)
+                w[k] = (n0 + k < N && c0 < C) ? __ldg(reinterpret_cast<const uint4*>(W + (size_t)(n0 + k) * C + c0))
+                                              : make_uint4(0, 0, 0, 0);
+            if (c0 < C) {
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) acc[r] = fmaf(wf[k], sc[r * C + c0 + k], acc[r]);
+                for (int k = 0; k < kAdaRowsPerWarp; ++k) {
+                    const float wf[8] = {bf16_lo(w[k].x), bf16_hi(w[k].x), bf16_lo(w[k].y), bf16_hi(w[k].y),
+                                         bf16_lo(w[k].z), bf16_hi(w[k].z), bf16_lo(w[k].w), bf16_hi(w[k].w)};
+#pragma unroll
+                    for (int r = 0; r < kAdaRChunk; ++r) {
+                        if (r < rc) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[k][r] = fmaf(wf[e], sc[r * C + c0 + e], acc[k][r]);
+                        }
                     }
                 }
             }
+        }
+#pragma unroll
+        for (int k = 0; k < kAdaRowsPerWarp; ++k) {
 #pragma unroll
             for (int r = 0; r < kAdaRChunk; ++r) {
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+                for (int off = 16; off > 0; off >>= 1) acc[k][r] += __shfl_xor_sync(0xffffffffu, acc[k][r], off);
             }
-            if (lane == 0) {
+            const int n = n0 + k;
+            if (lane == 0 && n < N) {
                 const float bn = bf16_lo(b[n]);
-                for (int r = 0; r < rc; ++r) mod[(size_t)(r0 + r) * N + n] = acc[r] + bn;
+                for (int r = 0; r < rc; ++r) mod[(size_t)(r0 + r) * N + n] = acc[k][r] + bn;
             }
         }
     }
@@ -129,7 +144,8 @@ int launch_adaln(const uint16_t* ada_w, const uint16_t* ada_b, const float* cond
     if (R <= 0 || C <= 0 || N <= 0) return set_error(DLO_ERR_INVALID_ARG, "adaln: non-positive size");
     if (C % 8) return set_error(DLO_ERR_ALIGNMENT, "adaln: cond_dim must be a multiple of 8");
     if (C > kAdaMaxC) return set_error(DLO_ERR_SHAPE, "adaln: cond_dim %d above %d", C, kAdaMaxC);
-    adaln_gemv<<<(N + 7) / 8, 256, 0, st>>>(ada_w, ada_b, cond, R, C, N, mod);
+    const int rows_per_cta = 8 * kAdaRowsPerWarp;
+    adaln_gemv<<<(N + rows_per_cta - 1) / rows_per_cta, 256, 0, st>>>(ada_w, ada_b, cond, R, C, N, mod);
     DLO_CUDA_TRY(cudaGetLastError());
     return DLO_OK;
 }
@@ -137,60 +153,71 @@ int launch_adaln(const uint16_t* ada_w, const uint16_t* ada_b, const float* cond
 // ------------------------------------------------------------------ LayerNorm + modulate
 
 constexpr int kLnThreads = 256;
-constexpr int kLnMaxVec = 8;  // float4 per thread: hidden <= 8192
+constexpr int kLnMaxVec = 8;  // float4 per thread
 
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float t = 0.f;
-#pragma unroll
-    for (int w = 0; w < kLnThreads / 32; ++w) t += red[w];
-    return t;
-}
-
-// One CTA per token row; the row stays in registers between the two passes.
+// A CTA of 256 threads normalises 256/TPR rows; each row is handled by TPR
+// threads (TPR chosen so a thread holds at most kLnMaxVec float4 of it), kept
+// in registers between the mean pass, the variance pass and the output pass.
+template <int TPR>
 __global__ void __launch_bounds__(kLnThreads) ln_modulate(const float* __restrict__ x, const float* __restrict__ shift,
-                                                          const float* __restrict__ scale, int mod_stride, int T,
-                                                          int hidden, uint16_t* __restrict__ u) {
-    __shared__ float red[kLnThreads / 32];
-    const int row = blockIdx.x;
-    const int req = row / T;
+                                                          const float* __restrict__ scale, int mod_stride, int rows,
+                                                          int T, int hidden, uint16_t* __restrict__ u) {
+    constexpr int kRowsPerCta = kLnThreads / TPR;
+    constexpr int kWarpsPerRow = TPR >= 32 ? TPR / 32 : 1;
+    __shared__ float red[2][kLnThreads / 32];
+    const int sub = threadIdx.x / TPR;       // row within the CTA
+    const int tid = threadIdx.x % TPR;       // thread within the row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kRowsPerCta + sub;
+    const bool live = row < rows;
     const int nvec = hidden / 4;
-    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)row * hidden);
+    const float4* xr = reinterpret_cast<const float4*>(x + (size_t)(live ? row : 0) * hidden);
     float4 v[kLnMaxVec];
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < kLnMaxVec; ++k) {
-        const int i = threadIdx.x + k * kLnThreads;
-        if (i < nvec) {
+        const int i = tid + k * TPR;
+        if (live && i < nvec) {
             v[k] = xr[i];
             s += (v[k].x + v[k].y) + (v[k].z + v[k].w);
         }
     }
-    const float mean = block_sum(s, red) / (float)hidden;
+    auto row_sum = [&](float val, int slot) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) val += __shfl_xor_sync(0xffffffffu, val, off);
+        if constexpr (kWarpsPerRow > 1) {
+            if (lane == 0) red[slot][warp] = val;
+            __syncthreads();
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarpsPerRow; ++w) t += red[slot][sub * kWarpsPerRow + w];
+            return t;
+        } else {
+            return val;
+        }
+    };
+    const float mean = row_sum(s, 0) / (float)hidden;
     float q = 0.f;
 #pragma unroll
     for (int k = 0; k < kLnMaxVec; ++k) {
-        const int i = threadIdx.x + k * kLnThreads;
-        if (i < nvec) {
-            const float a = v[k].x - mean, b = v[k].y - mean, c = v[k].z - mean, d = v[k].w - mean;
-            q += (a * a + b * b) + (c * c + d * d);
+        const int i = tid + k * TPR;
+        if (live && i < nvec) {
+            const float a = v[k].x - mean, bb = v[k].y - mean, c = v[k].z - mean, d = v[k].w - mean;
+            q += (a * a + bb * bb) + (c * c + d * d);
         }
     }
-    const float var = block_sum(q, red) / (float)hidden;
+    const float var = row_sum(q, 1) / (float)hidden;
+    if (!live) return;
     const float rstd = 1.0f / sqrtf(var + 1e-6f);
+    const int req = row / T;
     const float4* shr = reinterpret_cast<const float4*>(shift + (size_t)req * mod_stride);
     const float4* scr = reinterpret_cast<const float4*>(scale + (size_t)req * mod_stride);
     uint2* ur = reinterpret_cast<uint2*>(u + (size_t)row * hidden);
 #pragma unroll
     for (int k = 0; k < kLnMaxVec; ++k) {
-        const int i = threadIdx.x + k * kLnThreads;
+        const int i = tid + k * TPR;
         if (i < nvec) {
-            const float4 sh = shr[i], sc = scr[i];
+            const float4 sh = __ldg(shr + i), sc = __ldg(scr + i);
             uint2 o;
             o.x = pack_bf16x2((v[k].x - mean) * rstd * (1.f + sc.x) + sh.x, (v[k].y - mean) * rstd * (1.f + sc.y) + sh.y);
             o.y = pack_bf16x2((v[k].z - mean) * rstd * (1.f + sc.z) + sh.z, (v[k].w - mean) * rstd * (1.f + sc.w) + sh.w);
@@ -207,7 +234,18 @@ int launch_ln_modulate(const float* x, const float* shift, const float* scale, i
     if (hidden > kLnThreads * kLnMaxVec * 4) return set_error(DLO_ERR_SHAPE, "ln_modulate: hidden %d above 8192", hidden);
     const long rows = (long)R * T;
     if (rows > 0x7FFFFFFFL) return set_error(DLO_ERR_SHAPE, "ln_modulate: too many rows");
-    ln_modulate<<<(unsigned)rows, kLnThreads, 0, st>>>(x, shift, scale, mod_stride, T, hidden, u);
+    const int nvec = hidden / 4;
+    // fewest threads per row such that each holds at most kLnMaxVec float4
+    int tpr = 32;
+    while (tpr < kLnThreads && (nvec + tpr - 1) / tpr > kLnMaxVec) tpr *= 2;
+    const int rows_per_cta = kLnThreads / tpr;
+    const unsigned grid = (unsigned)((rows + rows_per_cta - 1) / rows_per_cta);
+    switch (tpr) {
+        case 32: ln_modulate<32><<<grid, kLnThreads, 0, st>>>(x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
+        case 64: ln_modulate<64><<<grid, kLnThreads, 0, st>>>(x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
+        case 128: ln_modulate<128><<<grid, kLnThreads, 0, st>>>(x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
+        default: ln_modulate<256><<<grid, kLnThreads, 0, st>>>(x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
+    }
     DLO_CUDA_TRY(cudaGetLastError());
     return DLO_OK;
 }
