@@ -259,18 +259,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ------------------------------------------------------------------ host side
 
 int gemm_block_n(int M, int N, int num_sms) {
-    // Estimated time ~ waves x per-tile time.  A 128-wide tile does half the
-    // MMA work of a 256-wide one but reloads the same A panel and keeps fewer
-    // bytes in flight per MMA; on GB300 a wave of them costs ~0.78 of a wave of
-    // 256-wide tiles.
+    // 256-wide tiles move fewer operand bytes per MMA and win whenever there
+    // are enough of them; measured on GB300 (T2I and Deep projection shapes)
+    // 128-wide tiles only win when the 256-wide tiling is short of 1.5 waves,
+    // where spreading the work over more SMs beats the higher per-tile cost.
     const long m_tiles = (M + kGemmBM - 1) / kGemmBM;
     const long t256 = m_tiles * ((N + 255) / 256);
-    const long t128 = m_tiles * ((N + 127) / 128);
-    const double w256 = (double)((t256 + num_sms - 1) / num_sms);
-    const double w128 = (double)((t128 + num_sms - 1) / num_sms);
-    const double cost256 = w256 * 1.0;
-    const double cost128 = w128 * 0.78;  // measured: a 128-wide wave costs ~0.78 of a 256-wide one
-    return cost128 < cost256 ? 128 : 256;
+    return (double)t256 < 1.5 * num_sms ? 128 : 256;
 }
 
 template <int BN, int EPI>
