@@ -71,7 +71,12 @@ enum {
     DLO_FILL_ZEROCOPY = 2,  /* shard-gather kernel reading mapped pinned memory, 16-byte loads */
     DLO_FILL_MASK = 3,
     DLO_RESIDENT = 1 << 4,  /* copy every block to the device once (no streaming); for checks */
-    DLO_PROFILE = 1 << 5    /* record CUDA events around every kernel (dlo_get_kernel_times) */
+    DLO_PROFILE = 1 << 5,   /* record CUDA events around every kernel (dlo_get_kernel_times) */
+    DLO_PREFETCH_NEXT = 1 << 6 /* at the end of each forward, start filling block 0 of the next call
+                                  into the slot block L-2 freed, so the next forward begins without
+                                  waiting for it (a diffusion loop runs the forward once per step);
+                                  the forward completes on its stream after that fill too; costs
+                                  one extra fill after the last call */
 };
 
 /* Shape of one DiT block.  head_dim = hidden / num_heads must be 64 or 128;

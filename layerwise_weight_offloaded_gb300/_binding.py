@@ -25,6 +25,7 @@ DLO_FILL_MEMCPY = 1
 DLO_FILL_ZEROCOPY = 2
 DLO_RESIDENT = 1 << 4
 DLO_PROFILE = 1 << 5
+DLO_PREFETCH_NEXT = 1 << 6
 
 DLO_NUM_PARAMS = 10
 PARAM_NAMES = ("ada_w", "ada_b", "qkv_w", "qkv_b", "proj_w", "proj_b", "fc1_w", "fc1_b", "fc2_w", "fc2_b")

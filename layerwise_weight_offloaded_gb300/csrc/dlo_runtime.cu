@@ -143,7 +143,10 @@ struct dlo_handle {
     int fill_mode = DLO_FILL_MEMCPY;
     bool resident = false;
     bool profile = false;
-    int status = DLO_OK;  // sticky error
+    bool prefetch = false;    // DLO_PREFETCH_NEXT
+    bool prefetched = false;  // block 0 of the next call is already being filled
+    int next_base = 0;        // slot of block 0 in the next call
+    int status = DLO_OK;      // sticky error
 
     std::vector<dlo_block_spec> specs;
     std::vector<int64_t> numel, S;
@@ -158,7 +161,7 @@ struct dlo_handle {
     uint16_t* slot[2] = {nullptr, nullptr};
     uint16_t* res_buf = nullptr;
     std::vector<int64_t> res_off;
-    std::vector<BlockMaps> maps;
+    std::vector<std::array<BlockMaps, 2>> maps;  // [block][slot]
 
     cudaStream_t copy = nullptr;
     cudaEvent_t filled[2] = {}, freed[2] = {}, start_ev = nullptr, done_ev = nullptr;
@@ -232,25 +235,29 @@ void prof_end(ProfEvent* e, cudaStream_t s) {
     if (e) cudaEventRecord(e->b, s);
 }
 
-int weights_base(dlo_handle* h, int b, const uint16_t** w) {
-    *w = h->resident ? h->res_buf + h->res_off[b] : h->slot[b & 1];
-    return DLO_OK;
+// Weights of block b: its region of the resident buffer, or the slot it runs from.
+const uint16_t* weights_base(const dlo_handle* h, int b, int slot) {
+    return h->resident ? h->res_buf + h->res_off[b] : h->slot[slot];
 }
 
+// Tensor maps of block b's four weight matrices in each slot it can run from
+// (the slot of a block rotates between calls when the next call's block 0 is
+// prefetched).
 int encode_block_maps(dlo_handle* h, int b) {
-    const uint16_t* w;
-    weights_base(h, b, &w);
     const auto& sp = h->specs[b];
     const auto& of = h->off[b];
     const uint64_t hd = sp.hidden, m = sp.mlp_hidden;
-    BlockMaps& bm = h->maps[b];
-    for (int v = 0; v < 2; ++v) {
-        const uint32_t box = v ? 256 : 128;
-        int rc;
-        if ((rc = encode_tmap_bf16(&bm.qkv[v], w + of[DLO_P_QKV_W], hd, 3 * hd, box))) return rc;
-        if ((rc = encode_tmap_bf16(&bm.proj[v], w + of[DLO_P_PROJ_W], hd, hd, box))) return rc;
-        if ((rc = encode_tmap_bf16(&bm.fc1[v], w + of[DLO_P_FC1_W], hd, m, box))) return rc;
-        if ((rc = encode_tmap_bf16(&bm.fc2[v], w + of[DLO_P_FC2_W], m, hd, box))) return rc;
+    for (int slot = 0; slot < (h->resident ? 1 : 2); ++slot) {
+        const uint16_t* w = weights_base(h, b, slot);
+        BlockMaps& bm = h->maps[b][slot];
+        for (int v = 0; v < 2; ++v) {
+            const uint32_t box = v ? 256 : 128;
+            int rc;
+            if ((rc = encode_tmap_bf16(&bm.qkv[v], w + of[DLO_P_QKV_W], hd, 3 * hd, box))) return rc;
+            if ((rc = encode_tmap_bf16(&bm.proj[v], w + of[DLO_P_PROJ_W], hd, hd, box))) return rc;
+            if ((rc = encode_tmap_bf16(&bm.fc1[v], w + of[DLO_P_FC1_W], hd, m, box))) return rc;
+            if ((rc = encode_tmap_bf16(&bm.fc2[v], w + of[DLO_P_FC2_W], m, hd, box))) return rc;
+        }
     }
     return DLO_OK;
 }
@@ -308,15 +315,15 @@ int ensure_activations(dlo_handle* h, int R, int T) {
     return DLO_OK;
 }
 
-// The kernels of one block, all on the compute stream `s`.
-int run_block(dlo_handle* h, int b, float* x, const float* cond, int R, int T, cudaStream_t s) {
+// The kernels of one block, weights read from `slot`, all on the compute stream `s`.
+int run_block(dlo_handle* h, int b, int slot, float* x, const float* cond, int R, int T, cudaStream_t s) {
     const auto& sp = h->specs[b];
     const auto& of = h->off[b];
     const int hd = sp.hidden, H = sp.num_heads, d = hd / H, m = sp.mlp_hidden, C = sp.cond_dim;
     const int M = R * T;
-    const uint16_t* w;
-    weights_base(h, b, &w);
-    const BlockMaps& bm = h->maps[b];
+    if (h->resident) slot = 0;
+    const uint16_t* w = weights_base(h, b, slot);
+    const BlockMaps& bm = h->maps[b][slot];
     const ActMaps& am = h->amaps[b];
     float* mod = h->mod;
     const int ms = 6 * hd;
@@ -420,7 +427,7 @@ int dlo_create(const dlo_block_spec* specs, int32_t num_blocks, int32_t dp_size,
     if (!specs || !shard_ptrs) return set_error(DLO_ERR_INVALID_ARG, "create: null specs or shard pointers");
     if (num_blocks < 1) return set_error(DLO_ERR_INVALID_ARG, "create: num_blocks must be >= 1");
     if (dp_size < 1 || dp_size > 64) return set_error(DLO_ERR_INVALID_ARG, "create: dp_size must be in [1, 64]");
-    if (flags & ~(uint32_t)(DLO_FILL_MASK | DLO_RESIDENT | DLO_PROFILE))
+    if (flags & ~(uint32_t)(DLO_FILL_MASK | DLO_RESIDENT | DLO_PROFILE | DLO_PREFETCH_NEXT))
         return set_error(DLO_ERR_INVALID_ARG, "create: unknown flag bits 0x%x", flags);
     if ((flags & DLO_FILL_MASK) == DLO_FILL_MASK) return set_error(DLO_ERR_INVALID_ARG, "create: bad fill mode");
 
@@ -433,6 +440,7 @@ int dlo_create(const dlo_block_spec* specs, int32_t num_blocks, int32_t dp_size,
     h->flags = flags;
     h->resident = (flags & DLO_RESIDENT) != 0;
     h->profile = (flags & DLO_PROFILE) != 0;
+    h->prefetch = (flags & DLO_PREFETCH_NEXT) != 0;
     h->specs.assign(specs, specs + num_blocks);
     h->numel.resize(num_blocks);
     h->S.resize(num_blocks);
@@ -564,21 +572,35 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
     do {                                                         \
         if ((e = (expr)) != cudaSuccess) return fail(h, cuda_error(e, #expr)); \
     } while (0)
+    // Block N runs from slot (base + N) % 2.  Without cross-call prefetch base is
+    // 0; with it, block 0 of this call was filled by the previous call into the
+    // slot its block L-2 had freed, and the slots alternate from there.
+    const bool prefetched = !h->resident && h->prefetched;
+    const int base = (!h->resident && h->prefetch) ? h->next_base : 0;
+    auto slot_of = [&](int N) { return (base + N) & 1; };
     if (!h->resident) {
-        // Slots may still be read by earlier work on `s`: the first fill waits for it.
-        FWD_TRY(cudaEventRecord(h->start_ev, s));
-        FWD_TRY(cudaStreamWaitEvent(h->copy, h->start_ev, 0));
-        ProfEvent* pe = prof_begin(h, DLO_K_FILL, h->copy);
-        if ((rc = issue_fill(h, 0, h->slot[0], h->fill_mode))) return fail(h, rc);
-        prof_end(pe, h->copy);
-        FWD_TRY(cudaEventRecord(h->filled[0], h->copy));
+        if (prefetched) {
+            // The activation scratch is shared: run after the previous forward
+            // (which may have been issued on another stream).
+            FWD_TRY(cudaStreamWaitEvent(s, h->done_ev, 0));
+        } else {
+            // Slots may still be read by earlier work on `s`: the first fill waits for it.
+            FWD_TRY(cudaEventRecord(h->start_ev, s));
+            FWD_TRY(cudaStreamWaitEvent(h->copy, h->start_ev, 0));
+            ProfEvent* pe = prof_begin(h, DLO_K_FILL, h->copy);
+            if ((rc = issue_fill(h, 0, h->slot[slot_of(0)], h->fill_mode))) return fail(h, rc);
+            prof_end(pe, h->copy);
+            FWD_TRY(cudaEventRecord(h->filled[slot_of(0)], h->copy));
+        }
     }
     for (int N = 0; N < h->L; ++N) {
-        const int slot = N & 1;
+        const int slot = slot_of(N);
         if (!h->resident) {
             if (N + 1 < h->L) {
-                const int ns = (N + 1) & 1;
-                if (N + 1 >= 2) FWD_TRY(cudaStreamWaitEvent(h->copy, h->freed[ns], 0));
+                const int ns = slot_of(N + 1);
+                // freed[ns] marks the end of the last block that read slot ns: block
+                // N-1 of this call, or the previous call's last block.
+                if (N + 1 >= 2 || prefetched) FWD_TRY(cudaStreamWaitEvent(h->copy, h->freed[ns], 0));
                 ProfEvent* pe = prof_begin(h, DLO_K_FILL, h->copy);
                 if ((rc = issue_fill(h, N + 1, h->slot[ns], h->fill_mode))) return fail(h, rc);
                 prof_end(pe, h->copy);
@@ -588,8 +610,23 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
             FWD_TRY(cudaStreamWaitEvent(s, h->filled[slot], 0));
             prof_end(pw, s);
         }
-        if ((rc = run_block(h, N, x, cond, R, T, s))) return fail(h, rc);
+        if ((rc = run_block(h, N, slot, x, cond, R, T, s))) return fail(h, rc);
         if (!h->resident) FWD_TRY(cudaEventRecord(h->freed[slot], s));
+    }
+    if (!h->resident && h->prefetch) {
+        // Fill block 0 of the next call into the slot block L-2 freed (the other
+        // slot still serves block L-1); the next call skips that fill.
+        const int nb = slot_of(h->L);
+        FWD_TRY(cudaStreamWaitEvent(h->copy, h->freed[nb], 0));
+        if ((rc = issue_fill(h, 0, h->slot[nb], h->fill_mode))) return fail(h, rc);
+        FWD_TRY(cudaEventRecord(h->filled[nb], h->copy));
+        // The forward completes on `stream` only once this fill has too: it runs
+        // beside block L-1 and is the next call's first wait anyway.
+        FWD_TRY(cudaStreamWaitEvent(s, h->filled[nb], 0));
+        h->next_base = nb;
+        h->prefetched = true;
+    } else {
+        h->prefetched = false;
     }
     FWD_TRY(cudaEventRecord(h->done_ev, s));
 #undef FWD_TRY
@@ -681,6 +718,7 @@ int dlo_debug_fill_and_read(dlo_handle* h, int32_t block, int32_t slot, void* ds
     int rc;
     cudaError_t e;
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail(h, cuda_error(e, "debug_fill: sync"));
+    h->prefetched = false;  // the slot written here may hold the next call's block 0
     if ((rc = issue_fill(h, block, h->slot[slot], h->fill_mode))) return fail(h, rc);
     if ((e = cudaStreamSynchronize(h->copy)) != cudaSuccess) return fail(h, cuda_error(e, "debug_fill: fill"));
     if ((e = cudaMemcpy(dst, h->slot[slot], (size_t)bytes, cudaMemcpyDeviceToHost)) != cudaSuccess)

@@ -120,6 +120,36 @@ def test_streamed_equals_resident_and_dp_invariant():
         assert np.array_equal(o.view(np.uint32), base.view(np.uint32)), name
 
 
+@pytest.mark.parametrize("L", [5, 4])
+def test_prefetch_next_call_bit_exact(L):
+    """With DLO_PREFETCH_NEXT each forward prefetches the next call's block 0;
+    consecutive calls (changing inputs and shapes, odd and even depth so the
+    slots rotate) give exactly what a handle without prefetch gives."""
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * L
+    plain = Run(specs, 3, 6, dlo.DLO_FILL_MEMCPY)
+    pre = Run(specs, 3, 6, dlo.DLO_FILL_MEMCPY | dlo.DLO_PREFETCH_NEXT)
+    try:
+        for i, (R, T) in enumerate([(1, 64), (2, 100), (1, 64), (3, 33)]):
+            x, c = inputs((R, T, cfg.hidden, cfg.cond_dim), 20 + i)
+            a = plain.forward(x, c)
+            b = pre.forward(x, c)
+            assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), (i, R, T)
+        st = dlo.dlo_get_stats(pre.h)
+        assert st["fills"] == 4 * L + 1  # every block once per call, plus the last prefetch
+        assert st["device_weight_high_water"] == 2 * st["slot_bytes"]
+        # a slot rewrite through the test accessor cancels the prefetch safely
+        n = dlo.dlo_block_numel(specs[0])
+        buf = np.empty(dlo.dlo_shard_numel(n, 3) * 3, np.uint16)
+        dlo.dlo_debug_fill_and_read(pre.h, 1, 0, buf, buf.nbytes)
+        dlo.dlo_debug_fill_and_read(pre.h, 1, 1, buf, buf.nbytes)
+        x, c = inputs((1, 64, cfg.hidden, cfg.cond_dim), 30)
+        assert np.array_equal(plain.forward(x, c), pre.forward(x, c))
+    finally:
+        plain.close()
+        pre.close()
+
+
 def test_zero_gates_identity_bit_exact():
     """ada_w = 0 and zero gate biases make every block the identity: x comes back unchanged."""
     cfg = synthetic.get_config("tiny")
