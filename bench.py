@@ -126,6 +126,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, dist=None, device: str = "cuda") -> float:
+    """The largest value of x over all ranks (replicas: the slowest rank sets the time)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job rate: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / seconds
+
+
 def cpu_info():
     model = ""
     try:
@@ -262,13 +277,9 @@ def main():
     step_ms = timed_steps(h, args.steps)
     clk = clocks.stop()
     launches = dlo.dlo_get_stats(h)["kernel_launches"] - launches0
-    ms_step = sum(step_ms) / args.steps
-    if dist:
-        t = torch.tensor([ms_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(sum(step_ms) / args.steps, dist)
     tokens = R * T
-    value = tokens * world / (ms_step * 1e-3)
+    value = job_throughput(tokens, world, ms_step * 1e-3)
 
     # cold: K forwards on a handle without the cross-call prefetch
     hc = dlo.dlo_create(specs, dp, ps.ptrs, dlo.dlo_get_stats(h)["fill_mode"])
@@ -309,11 +320,7 @@ def main():
         t0 = time.perf_counter()
         dlo.dlo_forward_host(h, xh, ch, R, T, stream)
         e2e_s.append(time.perf_counter() - t0)
-    e2e_step = float(np.median(e2e_s))
-    if dist:
-        t = torch.tensor([e2e_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_step = float(t.item())
+    e2e_step = max_over_ranks(float(np.median(e2e_s)), dist)
     st = dlo.dlo_get_stats(h)
 
     peaks, peak_src = measured_peaks()
@@ -366,7 +373,7 @@ def main():
                           "block_flops": gemm_f + attn_f + ada_f, "tensor_peak_tflops": p_tc / 1e12},
         "roofline": roofline,
         "cpu_baseline": cpu_base,
-        "e2e": {"value": tokens * world / e2e_step, "unit": "tokens/s",
+        "e2e": {"value": job_throughput(tokens, world, e2e_step), "unit": "tokens/s",
                 "h2d_bytes_per_step": xh.numel() * 4 + ch.numel() * 4, "d2h_bytes_per_step": xh.numel() * 4},
         "gpu_launches": launches,
         "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},

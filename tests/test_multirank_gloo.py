@@ -1,0 +1,66 @@
+"""The multi-rank path of bench.py on CPU: two gloo ranks.
+
+Every rank streams its own replica of the workload (no collective on the data
+path); the ranks only meet to time the job: the slowest rank's time, all ranks'
+units.  The reference arm runs on rank 0 alone.
+"""
+import contextlib
+import io
+import os
+import socket
+import sys
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        slowest = bench.max_over_ranks(10.0 + rank, dist, device="cpu")
+        rate = bench.job_throughput(4096, world, slowest * 1e-3)
+        dist.barrier()
+        # the reference arm: only rank 0 runs and prints
+        out = io.StringIO()
+        args = type("A", (), {"warmup": 0, "steps": 1})()
+        import synthetic
+        cfg = synthetic.get_config("tiny")
+        with contextlib.redirect_stdout(out):
+            bench.run_reference(args, cfg, rank, world)
+        q.put((rank, slowest, rate, out.getvalue()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_time_the_slowest_and_count_all_units():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = dict()
+    for _ in range(world):
+        rank, slowest, rate, printed = q.get(timeout=240)
+        results[rank] = (slowest, rate, printed)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank in range(world):
+        slowest, rate, printed = results[rank]
+        assert slowest == 11.0                       # max over ranks
+        assert rate == pytest.approx(4096 * 2 / 11e-3)  # all ranks' tokens / slowest time
+    assert '"impl": "reference"' in results[0][2]
+    assert results[1][2] == ""                       # other ranks do no work, print nothing
