@@ -141,6 +141,33 @@ def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
     return units_per_rank * world / seconds
 
 
+KERNEL_SOURCES = {"attention": "k_attention.cu", "gemm_qkv": "k_gemm.cu", "gemm_proj": "k_gemm.cu",
+                  "gemm_fc1": "k_gemm.cu", "gemm_fc2": "k_gemm.cu"}
+
+
+def profiled_traffic(kernel_class: str, workload: str):
+    """DRAM bytes per launch of `kernel_class` on `workload` from a committed ncu
+    summary under profiles/, or None when there is none or when the kernel's
+    source has changed since the counters were taken (hash recorded there)."""
+    import glob
+    import hashlib
+    src = os.path.join(ROOT, "layerwise_weight_offloaded_gb300", "csrc", KERNEL_SOURCES.get(kernel_class, ""))
+    if not os.path.isfile(src):
+        return None, None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        fields = {}
+        for line in open(path, encoding="utf-8"):
+            if ":" in line and not line.startswith(("|", "#", " ")):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+        if fields.get("kernel_class") == kernel_class and fields.get("workload") == workload:
+            if fields.get("source_sha256_16") == digest and fields.get("traffic_bytes_per_launch", "").isdigit():
+                return int(fields["traffic_bytes_per_launch"]), os.path.relpath(path, ROOT)
+            return None, os.path.relpath(path, ROOT) + " (kernel changed since capture)"
+    return None, None
+
+
 def cpu_info():
     model = ""
     try:
@@ -339,9 +366,11 @@ def main():
         dom = max(kf, key=lambda k: ktime[k])
         per_launch_s = ktime[dom] / max(klaunch[dom], 1) * 1e-3
         achieved = kf[dom] / per_launch_s / 1e12
+        traffic, traffic_src = profiled_traffic(dom, cfg.name)
         roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved,
                     "peak": p_tc / 1e12, "unit": "TFLOP/s", "frac": achieved / (p_tc / 1e12),
-                    "traffic": None,
+                    "traffic": traffic,
+                    "traffic_source": traffic_src,
                     "timing": "CUDA events around every launch, in a second timed pass of the same K steps",
                     "profiled_ms_per_step": sum(prof_step_ms) / max(len(prof_step_ms), 1),
                     "peak_source": f"bf16_tflops_sustained of {peak_src} peaks (kernel timed inside a long step)",

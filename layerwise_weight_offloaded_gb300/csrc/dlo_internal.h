@@ -38,6 +38,26 @@ int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_
 int encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
                         uint32_t box_rows);
 
+// Launches `kernel` with programmatic stream serialization: it may begin (and
+// run its prologue) while the previous kernel of the stream finishes.  The
+// kernel must call pdl_trigger() and pdl_wait() (dlo_device.cuh) before it
+// reads anything an earlier kernel wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Process-wide device error word for the single-op entry points.
 int op_error_flag(int** flag);
 

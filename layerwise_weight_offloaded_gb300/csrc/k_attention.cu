@@ -153,6 +153,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // prologue done: let the next kernel start its own, then wait for qkv
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -407,7 +410,8 @@ static int launch_attention_t(const uint16_t* qkv, int R, int T, int H, uint16_t
     if (rc) return rc;
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
     dim3 grid((T + 2 * kAttBM - 1) / (2 * kAttBM), H, R);
-    attention_fwd_tcgen05<D><<<grid, kAttThreads, Cfg::kSmemAlloc, st>>>(tm, T, H, o, scale_log2, err);
+    DLO_CUDA_TRY(launch_pdl(attention_fwd_tcgen05<D>, grid, dim3(kAttThreads), Cfg::kSmemAlloc, st, tm, T, H, o,
+                            scale_log2, err));
     DLO_CUDA_TRY(cudaGetLastError());
     return DLO_OK;
 }

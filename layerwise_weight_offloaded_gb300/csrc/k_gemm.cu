@@ -146,6 +146,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // prologue done: let the next kernel start its own, then wait for the
+    // previous kernel's outputs (A, the residual x, the modulation)
+    pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -283,7 +287,7 @@ static int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmW, const G
     }
     const int tiles = ((d.M + kGemmBM - 1) / kGemmBM) * ((d.N + BN - 1) / BN);
     const int grid = tiles < num_sms ? tiles : num_sms;
-    gemm_bf16_tcgen05<BN, EPI><<<grid, kGemmThreads, Cfg::kSmemBytes, st>>>(tmA, tmW, d);
+    DLO_CUDA_TRY(launch_pdl(gemm_bf16_tcgen05<BN, EPI>, dim3(grid), dim3(kGemmThreads), Cfg::kSmemBytes, st, tmA, tmW, d));
     DLO_CUDA_TRY(cudaGetLastError());
     return DLO_OK;
 }

@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(256) adaln_gemv(const uint16_t* __restrict__ W
                                                   const float* __restrict__ cond, int R, int C, int N,
                                                   float* __restrict__ mod) {
     __shared__ float sc[kAdaRChunk * kAdaMaxC];
+    pdl_trigger();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = (blockIdx.x * 8 + warp) * kAdaRowsPerWarp;
     const int steps = (C + 255) / 256;  // 8 weights per lane per step
@@ -145,7 +147,8 @@ int launch_adaln(const uint16_t* ada_w, const uint16_t* ada_b, const float* cond
     if (C % 8) return set_error(DLO_ERR_ALIGNMENT, "adaln: cond_dim must be a multiple of 8");
     if (C > kAdaMaxC) return set_error(DLO_ERR_SHAPE, "adaln: cond_dim %d above %d", C, kAdaMaxC);
     const int rows_per_cta = 8 * kAdaRowsPerWarp;
-    adaln_gemv<<<(N + rows_per_cta - 1) / rows_per_cta, 256, 0, st>>>(ada_w, ada_b, cond, R, C, N, mod);
+    DLO_CUDA_TRY(launch_pdl(adaln_gemv, dim3((N + rows_per_cta - 1) / rows_per_cta), dim3(256), 0, st, ada_w, ada_b,
+                            cond, R, C, N, mod));
     DLO_CUDA_TRY(cudaGetLastError());
     return DLO_OK;
 }
@@ -165,6 +168,8 @@ __global__ void __launch_bounds__(kLnThreads) ln_modulate(const float* __restric
     constexpr int kRowsPerCta = kLnThreads / TPR;
     constexpr int kWarpsPerRow = TPR >= 32 ? TPR / 32 : 1;
     __shared__ float red[2][kLnThreads / 32];
+    pdl_trigger();
+    pdl_wait();
     const int sub = threadIdx.x / TPR;       // row within the CTA
     const int tid = threadIdx.x % TPR;       // thread within the row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -240,12 +245,14 @@ int launch_ln_modulate(const float* x, const float* shift, const float* scale, i
     while (tpr < kLnThreads && (nvec + tpr - 1) / tpr > kLnMaxVec) tpr *= 2;
     const int rows_per_cta = kLnThreads / tpr;
     const unsigned grid = (unsigned)((rows + rows_per_cta - 1) / rows_per_cta);
+    cudaError_t e = cudaSuccess;
     switch (tpr) {
-        case 32: ln_modulate<32><<<grid, kLnThreads, 0, st>>>(x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
-        case 64: ln_modulate<64><<<grid, kLnThreads, 0, st>>>(x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
-        case 128: ln_modulate<128><<<grid, kLnThreads, 0, st>>>(x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
-        default: ln_modulate<256><<<grid, kLnThreads, 0, st>>>(x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
+        case 32: e = launch_pdl(ln_modulate<32>, dim3(grid), dim3(kLnThreads), 0, st, x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
+        case 64: e = launch_pdl(ln_modulate<64>, dim3(grid), dim3(kLnThreads), 0, st, x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
+        case 128: e = launch_pdl(ln_modulate<128>, dim3(grid), dim3(kLnThreads), 0, st, x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
+        default: e = launch_pdl(ln_modulate<256>, dim3(grid), dim3(kLnThreads), 0, st, x, shift, scale, mod_stride, (int)rows, T, hidden, u); break;
     }
+    DLO_CUDA_TRY(e);
     DLO_CUDA_TRY(cudaGetLastError());
     return DLO_OK;
 }
