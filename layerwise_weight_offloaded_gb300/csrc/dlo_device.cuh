@@ -155,25 +155,42 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int M, int N) {
            | ((uint32_t)(M >> 4) << 24);        // M / 16
 }
 
-// D[tmem] (+)= A[smem] . B[smem]^T, issued by one thread.
+// tcgen05.mma and tcgen05.commit below are called by all 32 lanes of a
+// converged warp and issued by the one lane elect.sync picks (the same lane
+// every time, since the whole warp takes part).  Keeping the issuing warp
+// converged lets its addresses and descriptors stay warp-uniform, which makes
+// back-to-back issue several times cheaper than from a lone diverged lane.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, e;\n\t}"
+        : "=r"(e));
+    return e != 0;
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
 // D[tmem] (+)= A[tmem] . B[smem]^T: A (M x K bf16) read from TMEM, row i in
-// lane i, two K elements per 32-bit column; issued by one thread.
+// lane i, two K elements per 32-bit column.
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                              uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -185,11 +202,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// Arrive once on `bar` when every tcgen05 op this thread issued so far is done.
+// Arrive once on `bar` when every tcgen05.mma the warp's elected lane issued
+// so far is done (called by the whole warp, like umma_bf16).
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
 }
 
 // Each lane of the warp reads 32 consecutive 32-bit columns of its TMEM lane.

@@ -83,9 +83,10 @@ struct GemmArgs {
     int T;
     int* err;
 };
-// Tensor maps from encode_tmap_bf16: A over [M, K] with box rows 128; tmW[0]
-// and tmW[1] over W [N, K] with box rows 128 and 256 (the kernel picks its
-// tile width per shape).
+// Tensor maps from encode_tmap_bf16: A over [M, K] with box rows 128; the two
+// W [N, K] maps from encode_gemm_w_maps (the kernel picks its tile width per
+// shape and loads the W tile as one 256-row box or two or three 64-row boxes).
+int encode_gemm_w_maps(CUtensorMap* tmW, const void* W, uint64_t N, uint64_t K);
 int gemm_block_n(int M, int N, int num_sms);
 int launch_gemm(const CUtensorMap& tmA, const CUtensorMap* tmW, const GemmArgs& a, cudaStream_t st, int num_sms);
 

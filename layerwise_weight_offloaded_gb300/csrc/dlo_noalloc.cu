@@ -77,8 +77,7 @@ extern "C" int dlo_op_linear_noalloc(int32_t epilogue, const uint16_t* A, const 
     if ((rc = noalloc_scratch(&scratch))) return rc;
     CUtensorMap ta, tw[2];
     if ((rc = encode_tmap_bf16(&ta, A, (uint64_t)K, (uint64_t)M, 128))) return rc;
-    if ((rc = encode_tmap_bf16(&tw[0], W, (uint64_t)K, (uint64_t)N, 128))) return rc;
-    if ((rc = encode_tmap_bf16(&tw[1], W, (uint64_t)K, (uint64_t)N, 256))) return rc;
+    if ((rc = encode_gemm_w_maps(tw, W, (uint64_t)N, (uint64_t)K))) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     DLO_CUDA_TRY(cudaMemsetAsync(scratch, 0, kNoallocWordsPerCall * sizeof(int), s));
     GemmArgs a{epilogue, M, N, K, bias, out, gate, gate_stride, T, scratch};

@@ -85,6 +85,11 @@ int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return DLO_OK;
 }
 
+int encode_gemm_w_maps(CUtensorMap* tmW, const void* W, uint64_t N, uint64_t K) {
+    int rc = encode_tmap_bf16(&tmW[0], W, K, N, 64);
+    return rc ? rc : encode_tmap_bf16(&tmW[1], W, K, N, 256);
+}
+
 int encode_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
                         uint32_t box_rows) {
     auto enc = tmap_encoder();
@@ -123,7 +128,7 @@ int op_error_flag(int** flag) {
 
 using namespace dlo;
 
-// Weight tensor maps of one block in the slot it runs from (box 128 and 256 rows).
+// Weight tensor maps of one block in the slot it runs from (encode_gemm_w_maps).
 struct BlockMaps {
     CUtensorMap qkv[2], proj[2], fc1[2], fc2[2];
 };
@@ -250,14 +255,11 @@ int encode_block_maps(dlo_handle* h, int b) {
     for (int slot = 0; slot < (h->resident ? 1 : 2); ++slot) {
         const uint16_t* w = weights_base(h, b, slot);
         BlockMaps& bm = h->maps[b][slot];
-        for (int v = 0; v < 2; ++v) {
-            const uint32_t box = v ? 256 : 128;
-            int rc;
-            if ((rc = encode_tmap_bf16(&bm.qkv[v], w + of[DLO_P_QKV_W], hd, 3 * hd, box))) return rc;
-            if ((rc = encode_tmap_bf16(&bm.proj[v], w + of[DLO_P_PROJ_W], hd, hd, box))) return rc;
-            if ((rc = encode_tmap_bf16(&bm.fc1[v], w + of[DLO_P_FC1_W], hd, m, box))) return rc;
-            if ((rc = encode_tmap_bf16(&bm.fc2[v], w + of[DLO_P_FC2_W], m, hd, box))) return rc;
-        }
+        int rc;
+        if ((rc = encode_gemm_w_maps(bm.qkv, w + of[DLO_P_QKV_W], 3 * hd, hd))) return rc;
+        if ((rc = encode_gemm_w_maps(bm.proj, w + of[DLO_P_PROJ_W], hd, hd))) return rc;
+        if ((rc = encode_gemm_w_maps(bm.fc1, w + of[DLO_P_FC1_W], m, hd))) return rc;
+        if ((rc = encode_gemm_w_maps(bm.fc2, w + of[DLO_P_FC2_W], hd, m))) return rc;
     }
     return DLO_OK;
 }
@@ -771,8 +773,7 @@ int dlo_op_linear(int32_t epilogue, const uint16_t* A, const uint16_t* W, const 
     if ((rc = op_error_flag(&err))) return rc;
     CUtensorMap ta, tw[2];
     if ((rc = encode_tmap_bf16(&ta, A, (uint64_t)K, (uint64_t)M, 128))) return rc;
-    if ((rc = encode_tmap_bf16(&tw[0], W, (uint64_t)K, (uint64_t)N, 128))) return rc;
-    if ((rc = encode_tmap_bf16(&tw[1], W, (uint64_t)K, (uint64_t)N, 256))) return rc;
+    if ((rc = encode_gemm_w_maps(tw, W, (uint64_t)N, (uint64_t)K))) return rc;
     GemmArgs a{epilogue, M, N, K, bias, out, gate, gate_stride, T, err};
     return launch_gemm(ta, tw, a, reinterpret_cast<cudaStream_t>(stream), d.num_sms);
 }

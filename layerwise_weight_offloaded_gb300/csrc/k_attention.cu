@@ -6,16 +6,17 @@
 // O = softmax(Q K^T / sqrt(d)) V: fp32 logits in TMEM, fp32 online softmax,
 // softmax weights rounded to bf16 for the P.V product, fp32 accumulation.
 //
-// One CTA = two 128-row query tiles of one (request, head), 10 warps:
+// One CTA = two 128-row query tiles of one (request, head), 12 warps:
 //   warp 0     TMA producer: both Q tiles once, then 128-key K and V tiles into
 //              a STAGES-deep ring shared by the two query tiles (3-D tensor map
 //              over [R, T, 3h]: a tile never reaches into the next request,
 //              rows past T read zero);
-//   warp 1     allocates all 512 TMEM columns; lane 0 issues, per key tile j
-//              and query tile t, S(t,j) = Q_t K_j^T (both operands K-major
-//              from shared memory) and O_t += P(t,j) V_j with P read from TMEM
-//              and V MN-major straight from its TMA tile;
-//   warps 2-5  softmax of query tile 0, warps 6-9 of query tile 1: one query
+//   warp 1     allocates all 512 TMEM columns and issues, per key tile j and
+//              query tile t, S(t,j) = Q_t K_j^T (both operands K-major from
+//              shared memory) and O_t += P(t,j) V_j with P read from TMEM and V
+//              MN-major straight from its TMA tile;
+//   warps 2-3  idle after the prologue;
+//   warps 4-7  softmax of query tile 0, warps 8-11 of query tile 1: one query
 //              row per thread (warp w owns TMEM lanes 32*(w%4)..+31).  Each
 //              tcgen05.ld's the S row, masks keys past T, keeps the running
 //              max m and sum l, and writes P = 2^(S*c - m) as packed bf16 back
@@ -26,6 +27,10 @@
 //              instructions and the max a 3-input max, so a thread spends about
 //              three instructions per logit besides the exponential.  At the
 //              end each thread writes its row of O / l.
+// The producer and MMA warps run converged, one elected lane issuing each copy
+// and MMA: issuing from a lone diverged lane cost ~80 cycles per MMA and left
+// the tensor core waiting on its issuer.  Warps 0-3 give registers back
+// (setmaxnreg) so the softmax warps hold a whole 128-logit row without spills.
 // The tensor core alternates between the two query tiles, so one tile's
 // MMAs run while the other tile's softmax does.
 //   d = 64 : TMEM per tile [S 128 | P 64 | O 64]; the softmax frees S as soon
@@ -45,7 +50,15 @@ namespace {
 
 constexpr int kAttBM = 128;   // query rows per tile (two tiles per CTA)
 constexpr int kAttBN = 128;   // keys per tile
-constexpr int kAttThreads = 320;
+constexpr int kAttThreads = 384;
+// Register split after the prologue: warps 0-3 drop to kRegsControl, the two
+// softmax warpgroups rise to kRegsSoftmax.  __launch_bounds__(384, 1) gives
+// every thread 168 registers at launch (65536 / 384, rounded down to 8); the
+// split must not ask for more than that launch total.
+constexpr int kRegsControl = 88;
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsAtLaunch = 168;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kAttThreads * kRegsAtLaunch, "register split over budget");
 constexpr int kTileBytes = 128 * 128;  // one 128-row x 64-col bf16 box = 16 KB
 constexpr float kLazyRescale = 8.0f;   // log2 units
 
@@ -157,41 +170,50 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     pdl_trigger();
     pdl_wait();
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer
+    const unsigned FULL = 0xffffffffu;
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+        if (warp == 0) {
+            // ---------------- TMA producer (whole warp; one elected lane issues)
             long issued_k = 0, issued_v = 0;
-            mbar_arrive_expect_tx(q_full, 2 * Cfg::kQBytes);
-            for (int t = 0; t < 2; ++t)
-                for (int c = 0; c < Cfg::kChunks; ++c)
-                    tma_load_3d(sQ + t * Cfg::kQBytes + c * kTileBytes, &tm, head * D + c * 64, q0 + t * kAttBM, req,
-                                q_full);
+            if (elect_one()) {
+                mbar_arrive_expect_tx(q_full, 2 * Cfg::kQBytes);
+                for (int t = 0; t < 2; ++t)
+                    for (int c = 0; c < Cfg::kChunks; ++c)
+                        tma_load_3d(sQ + t * Cfg::kQBytes + c * kTileBytes, &tm, head * D + c * 64, q0 + t * kAttBM,
+                                    req, q_full);
+            }
+            __syncwarp();
             for (int j = 0; j < n_kv; ++j) {
                 const int s = j % ST;
                 const uint32_t ph = (uint32_t)((j / ST) & 1);
-                if (!mbar_wait_bounded(&k_empty[s], ph ^ 1u, err, KERR_ATT_PRODUCER)) break;
-                mbar_arrive_expect_tx(&k_full[s], Cfg::kKVBytes);
-                for (int c = 0; c < Cfg::kChunks; ++c)
-                    tma_load_3d(sK + s * Cfg::kKVBytes + c * kTileBytes, &tm, h + head * D + c * 64, j * kAttBN, req,
-                                &k_full[s]);
+                if (!__all_sync(FULL, mbar_wait_bounded(&k_empty[s], ph ^ 1u, err, KERR_ATT_PRODUCER))) break;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&k_full[s], Cfg::kKVBytes);
+                    for (int c = 0; c < Cfg::kChunks; ++c)
+                        tma_load_3d(sK + s * Cfg::kKVBytes + c * kTileBytes, &tm, h + head * D + c * 64, j * kAttBN,
+                                    req, &k_full[s]);
+                }
+                __syncwarp();
                 ++issued_k;
-                if (!mbar_wait_bounded(&v_empty[s], ph ^ 1u, err, KERR_ATT_PRODUCER)) break;
-                mbar_arrive_expect_tx(&v_full[s], Cfg::kKVBytes);
-                for (int c = 0; c < Cfg::kChunks; ++c)
-                    tma_load_3d(sV + s * Cfg::kKVBytes + c * kTileBytes, &tm, 2 * h + head * D + c * 64, j * kAttBN,
-                                req, &v_full[s]);
+                if (!__all_sync(FULL, mbar_wait_bounded(&v_empty[s], ph ^ 1u, err, KERR_ATT_PRODUCER))) break;
+                if (elect_one()) {
+                    mbar_arrive_expect_tx(&v_full[s], Cfg::kKVBytes);
+                    for (int c = 0; c < Cfg::kChunks; ++c)
+                        tma_load_3d(sV + s * Cfg::kKVBytes + c * kTileBytes, &tm, 2 * h + head * D + c * 64,
+                                    j * kAttBN, req, &v_full[s]);
+                }
+                __syncwarp();
                 ++issued_v;
             }
             // every copy started here lands before the CTA exits
-            mbar_wait_bounded(q_full, 0, err, KERR_ATT_DRAIN);
+            __all_sync(FULL, mbar_wait_bounded(q_full, 0, err, KERR_ATT_DRAIN));
             for (long j = issued_k > ST ? issued_k - ST : 0; j < issued_k; ++j)
-                mbar_wait_bounded(&k_full[j % ST], (uint32_t)((j / ST) & 1), err, KERR_ATT_DRAIN);
+                __all_sync(FULL, mbar_wait_bounded(&k_full[j % ST], (uint32_t)((j / ST) & 1), err, KERR_ATT_DRAIN));
             for (long j = issued_v > ST ? issued_v - ST : 0; j < issued_v; ++j)
-                mbar_wait_bounded(&v_full[j % ST], (uint32_t)((j / ST) & 1), err, KERR_ATT_DRAIN);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
+                __all_sync(FULL, mbar_wait_bounded(&v_full[j % ST], (uint32_t)((j / ST) & 1), err, KERR_ATT_DRAIN));
+        } else if (warp == 1) {
+            // ---------------- MMA issuer (whole warp; one elected lane issues)
             constexpr uint32_t idesc_s = umma_idesc_bf16_f32(kAttBM, kAttBN);
             constexpr uint32_t idesc_pv = umma_idesc_bf16_f32(kAttBM, D) | (1u << 16);  // B (= V) MN-major
             // S(t, j) = Q_t K_j^T into tile t's S columns
@@ -216,8 +238,10 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                                  (j > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&o_done[t]);
             };
-            bool ok = mbar_wait_bounded(q_full, 0, err, KERR_ATT_MMA) &&
-                      mbar_wait_bounded(&k_full[0], 0, err, KERR_ATT_MMA);
+            auto wait = [&](uint64_t* bar, uint32_t parity) {
+                return __all_sync(FULL, mbar_wait_bounded(bar, parity, err, KERR_ATT_MMA));
+            };
+            bool ok = wait(q_full, 0) && wait(&k_full[0], 0);
             if (ok) {
                 tc_fence_after();
                 issue_s(0, 0);
@@ -228,20 +252,19 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 const uint32_t ph = (uint32_t)(j & 1);
                 const bool next = j + 1 < n_kv;
                 const int sn = (j + 1) % ST;
-                if (next && !(ok = mbar_wait_bounded(&k_full[sn], (uint32_t)(((j + 1) / ST) & 1), err, KERR_ATT_MMA)))
-                    break;
-                if (!(ok = mbar_wait_bounded(&v_full[j % ST], (uint32_t)((j / ST) & 1), err, KERR_ATT_MMA))) break;
+                if (next && !(ok = wait(&k_full[sn], (uint32_t)(((j + 1) / ST) & 1)))) break;
+                if (!(ok = wait(&v_full[j % ST], (uint32_t)((j / ST) & 1)))) break;
                 if constexpr (!Cfg::kAliasP) {
                     // per query tile: S(t, j+1) once softmax(t, j) has loaded S(t, j),
                     // then PV(t, j) once it has written P; the two tiles do not wait
                     // on each other
                     for (int t = 0; t < 2 && ok; ++t) {
                         if (next) {
-                            if (!(ok = mbar_wait_bounded(&s_free[t], ph, err, KERR_ATT_MMA))) break;
+                            if (!(ok = wait(&s_free[t], ph))) break;
                             tc_fence_after();
                             issue_s(t, j + 1);
                         }
-                        if (!(ok = mbar_wait_bounded(&p_full[t], ph, err, KERR_ATT_MMA))) break;
+                        if (!(ok = wait(&p_full[t], ph))) break;
                         tc_fence_after();
                         issue_pv(t, j);
                     }
@@ -249,15 +272,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 } else {
                     // P lives in S's columns: S(t, j+1) is issued only once PV(t, j),
                     // which reads P there, has completed.  Both PVs are queued first so
-                    // the tensor core stays busy while this thread waits.
+                    // the tensor core stays busy while this warp waits.
                     for (int t = 0; t < 2 && ok; ++t) {
-                        if (!(ok = mbar_wait_bounded(&p_full[t], ph, err, KERR_ATT_MMA))) break;
+                        if (!(ok = wait(&p_full[t], ph))) break;
                         tc_fence_after();
                         issue_pv(t, j);
                     }
                     if (ok && next) {
                         for (int t = 0; t < 2 && ok; ++t) {
-                            if (!(ok = mbar_wait_bounded(&o_done[t], ph, err, KERR_ATT_MMA))) break;
+                            if (!(ok = wait(&o_done[t], ph))) break;
                             tc_fence_after();
                             issue_s(t, j + 1);
                         }
@@ -267,19 +290,19 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 if (ok) umma_commit(&v_empty[j % ST]);
             }
             umma_commit(drain);
-            mbar_wait_bounded(drain, 0, err, KERR_ATT_DRAIN);
+            __all_sync(FULL, mbar_wait_bounded(drain, 0, err, KERR_ATT_DRAIN));
         }
     } else {
-        // ---------------- softmax warpgroups: warps 2-5 tile 0, warps 6-9 tile 1.
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+        // ---------------- softmax warpgroups: warps 4-7 tile 0, warps 8-11 tile 1.
         // All control flow around tcgen05.ld/st is uniform across the warp.
-        const int t = warp >= 6 ? 1 : 0;
+        const int t = warp >= 8 ? 1 : 0;
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const uint32_t s_addr = tmem + lane_base + Cfg::s_col(t);
         const uint32_t p_addr = tmem + lane_base + Cfg::p_col(t);
         const uint32_t o_addr = tmem + lane_base + Cfg::o_col(t);
-        const unsigned FULL = 0xffffffffu;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
@@ -402,6 +425,13 @@ static int launch_attention_t(const uint16_t* qkv, int R, int T, int H, uint16_t
     if (!configured[dev]) {
         DLO_CUDA_TRY(cudaFuncSetAttribute(attention_fwd_tcgen05<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           Cfg::kSmemAlloc));
+        // the setmaxnreg split assumes the launch register count; refuse to
+        // launch a build that allocated fewer (the increase would never be met)
+        cudaFuncAttributes fa;
+        DLO_CUDA_TRY(cudaFuncGetAttributes(&fa, attention_fwd_tcgen05<D>));
+        if (fa.numRegs < kRegsAtLaunch)
+            return set_error(DLO_ERR_UNSUPPORTED, "attention: kernel built with %d registers per thread, needs %d",
+                             fa.numRegs, kRegsAtLaunch);
         configured[dev] = true;
     }
     CUtensorMap tm;

@@ -6,11 +6,13 @@
 // rebuilt buffer).  Both operands are K-major, fp32 accumulation in TMEM.
 //
 // Persistent kernel, one CTA per SM, 10 warps:
-//   warp 0     TMA producer: 128x64 A box and BNx64 W box per stage into a
+//   warp 0     TMA producer: 128x64 A box and the BNx64 W tile (one 256-row
+//              box, or two or three 64-row boxes) per stage into a
 //              STAGES-deep shared-memory ring (128-byte swizzle);
-//   warp 1     allocates 2*BN TMEM columns; lane 0 issues tcgen05.mma
-//              (M=128, N=BN, K=16 per instruction) and commits each stage back
-//              to the producer and each finished tile to the epilogue;
+//   warp 1     allocates 2*BN TMEM columns and issues tcgen05.mma (M=128,
+//              N=BN, K=16 per instruction), committing each stage back to the
+//              producer and each finished tile to the epilogue;
+//              both run converged, one elected lane issuing each copy or MMA;
 //   warps 2-9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
 //              lanes 32*(w%4)..+31 = its 32 rows; warps 2-5 take the first
 //              half of the tile's columns, warps 6-9 the second), bias + GELU
@@ -28,17 +30,21 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmBK = 64;
 constexpr int kGemmThreads = 320;
 constexpr int kGemmEpiThreads = 256;
+constexpr unsigned kFullMask = 0xffffffffu;
 
 template <int BN>
 struct GemmCfg {
-    static constexpr int kStages = BN == 256 ? 4 : 6;
+    static_assert(BN == 128 || BN == 192 || BN == 256, "tile widths 128, 192, 256");
+    static constexpr int kStages = BN == 256 ? 4 : BN == 192 ? 5 : 6;
     static constexpr int kABytes = kGemmBM * kGemmBK * 2;
     static constexpr int kBBytes = BN * kGemmBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kWBox = BN == 256 ? 256 : 64;  // rows per W copy (the W map's box)
+    static constexpr int kTmemCols = BN == 128 ? 256 : 512;  // two accumulators, power of two
     static constexpr int kBarBytes = 256;
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + kBarBytes;
-    static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
+    static_assert(2 * BN <= kTmemCols && kTmemCols <= 512, "TMEM holds 512 columns");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
 struct GemmDevArgs {
@@ -152,77 +158,79 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     pdl_wait();
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer
-            int stage = 0;
-            uint32_t phase = 0;
-            long issued = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                const int m0 = (tile % num_m) * kGemmBM;
-                const int n0 = (tile / num_m) * BN;
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.err, KERR_GEMM_PRODUCER)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* sa = smem + stage * Cfg::kStageBytes;
+        // ---------------- TMA producer (whole warp; one elected lane issues)
+        int stage = 0;
+        uint32_t phase = 0;
+        long issued = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            const int m0 = (tile % num_m) * kGemmBM;
+            const int n0 = (tile / num_m) * BN;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!__all_sync(kFullMask, mbar_wait_bounded(&empty[stage], phase ^ 1u, p.err, KERR_GEMM_PRODUCER))) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sa = smem + stage * Cfg::kStageBytes;
+                if (elect_one()) {
                     mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
                     tma_load_2d(sa, &tmA, kb * kGemmBK, m0, &full[stage]);
-                    tma_load_2d(sa + Cfg::kABytes, &tmW, kb * kGemmBK, n0, &full[stage]);
-                    ++issued;
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            // Every copy this thread started must land before the CTA exits.
-            const long first = issued > S ? issued - S : 0;
-            for (long j = first; j < issued; ++j)
-                mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), p.err, KERR_GEMM_DRAIN);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
-            constexpr uint32_t idesc = umma_idesc_bf16_f32(kGemmBM, BN);
-            int stage = 0;
-            uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, p.err, KERR_GEMM_MMA)) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait_bounded(&full[stage], phase, p.err, KERR_GEMM_MMA)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_addr = smem_u32(smem + stage * Cfg::kStageBytes);
-                    const uint32_t b_addr = a_addr + Cfg::kABytes;
 #pragma unroll
-                    for (int k = 0; k < kGemmBK / 16; ++k) {
-                        umma_bf16(d_tmem, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32), idesc,
-                                  (kb | k) != 0);
-                    }
-                    umma_commit(&empty[stage]);  // stage is free once these MMAs have read it
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    for (int w = 0; w < BN / Cfg::kWBox; ++w)
+                        tma_load_2d(sa + Cfg::kABytes + w * Cfg::kWBox * kGemmBK * 2, &tmW, kb * kGemmBK,
+                                    n0 + w * Cfg::kWBox, &full[stage]);
                 }
-                if (!ok) break;
-                umma_commit(&acc_full[acc]);
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
+                __syncwarp();
+                ++issued;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
-            // All MMAs issued here must finish before TMEM is released.
-            umma_commit(drain);
-            mbar_wait_bounded(drain, 0, p.err, KERR_GEMM_DRAIN);
         }
+        // Every copy this warp started must land before the CTA exits.
+        const long first = issued > S ? issued - S : 0;
+        for (long j = first; j < issued; ++j)
+            __all_sync(kFullMask, mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1), p.err, KERR_GEMM_DRAIN));
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (whole warp; one elected lane issues)
+        constexpr uint32_t idesc = umma_idesc_bf16_f32(kGemmBM, BN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            if (!__all_sync(kFullMask, mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1u, p.err, KERR_GEMM_MMA))) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!__all_sync(kFullMask, mbar_wait_bounded(&full[stage], phase, p.err, KERR_GEMM_MMA))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(smem + stage * Cfg::kStageBytes);
+                const uint32_t b_addr = a_addr + Cfg::kABytes;
+#pragma unroll
+                for (int k = 0; k < kGemmBK / 16; ++k) {
+                    umma_bf16(d_tmem, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32), idesc,
+                              (kb | k) != 0);
+                }
+                umma_commit(&empty[stage]);  // stage is free once these MMAs have read it
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit(&acc_full[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        // All MMAs issued here must finish before TMEM is released.
+        umma_commit(drain);
+        __all_sync(kFullMask, mbar_wait_bounded(drain, 0, p.err, KERR_GEMM_DRAIN));
     } else {
         // ---------------- epilogue warps 2..9
         const int quarter = warp & 3;
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int m0 = (tile % num_m) * kGemmBM;
             const int n0 = (tile / num_m) * BN;
             // uniform across the warp: the tcgen05.ld below is warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[acc], acc_phase, p.err, KERR_GEMM_EPILOGUE)))
+            if (!__all_sync(kFullMask, mbar_wait_bounded(&acc_full[acc], acc_phase, p.err, KERR_GEMM_EPILOGUE)))
                 break;
             tc_fence_after();
             const int row = m0 + row_in_tile;
@@ -263,13 +271,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ------------------------------------------------------------------ host side
 
 int gemm_block_n(int M, int N, int num_sms) {
-    // 256-wide tiles move fewer operand bytes per MMA and win whenever there
-    // are enough of them; measured on GB300 (T2I and Deep projection shapes)
-    // 128-wide tiles only win when the 256-wide tiling is short of 1.5 waves,
-    // where spreading the work over more SMs beats the higher per-tile cost.
+    // Tiles are 128 x BN; a persistent CTA per SM walks them, so the time is
+    // about (waves of tiles) x BN x (cost of a tile column at that width).
+    // Narrower tiles re-read A more often and feed the tensor core from
+    // shared memory at a higher byte rate per FLOP: measured on GB300 (T2I and
+    // Deep projection shapes) a 192-wide column costs ~4% and a 128-wide one
+    // ~12% more than a 256-wide one.  Ties go to the wider tile.
+    static const int kWidths[3] = {256, 192, 128};
+    static const double kColumnCost[3] = {1.0, 1.04, 1.12};
     const long m_tiles = (M + kGemmBM - 1) / kGemmBM;
-    const long t256 = m_tiles * ((N + 255) / 256);
-    return (double)t256 < 1.5 * num_sms ? 128 : 256;
+    int best = 256;
+    double best_t = 0;
+    for (int i = 0; i < 3; ++i) {
+        const long tiles = m_tiles * ((N + kWidths[i] - 1) / kWidths[i]);
+        const long waves = (tiles + num_sms - 1) / num_sms;
+        const double t = (double)waves * kWidths[i] * kColumnCost[i];
+        if (i == 0 || t < best_t) {
+            best = kWidths[i];
+            best_t = t;
+        }
+    }
+    return best;
 }
 
 template <int BN, int EPI>
@@ -301,14 +323,19 @@ int launch_gemm(const CUtensorMap& tmA, const CUtensorMap* tmWs, const GemmArgs&
     GemmDevArgs d{a.M, a.N, a.K, a.bias, a.out, a.gate, a.gate_stride, a.T, a.err};
     const int bn = gemm_block_n(a.M, a.N, num_sms);
     const CUtensorMap& tmW = tmWs[bn == 256 ? 1 : 0];
-    switch (a.epilogue * 2 + (bn == 256 ? 1 : 0)) {
-        case DLO_EPI_BIAS * 2: return launch_gemm_t<128, DLO_EPI_BIAS>(tmA, tmW, d, st, num_sms);
-        case DLO_EPI_BIAS * 2 + 1: return launch_gemm_t<256, DLO_EPI_BIAS>(tmA, tmW, d, st, num_sms);
-        case DLO_EPI_BIAS_GELU * 2: return launch_gemm_t<128, DLO_EPI_BIAS_GELU>(tmA, tmW, d, st, num_sms);
-        case DLO_EPI_BIAS_GELU * 2 + 1: return launch_gemm_t<256, DLO_EPI_BIAS_GELU>(tmA, tmW, d, st, num_sms);
-        case DLO_EPI_GATED_RESIDUAL * 2:
+    const int wi = bn == 128 ? 0 : bn == 192 ? 1 : 2;
+    switch (a.epilogue * 3 + wi) {
+        case DLO_EPI_BIAS * 3 + 0: return launch_gemm_t<128, DLO_EPI_BIAS>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_BIAS * 3 + 1: return launch_gemm_t<192, DLO_EPI_BIAS>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_BIAS * 3 + 2: return launch_gemm_t<256, DLO_EPI_BIAS>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_BIAS_GELU * 3 + 0: return launch_gemm_t<128, DLO_EPI_BIAS_GELU>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_BIAS_GELU * 3 + 1: return launch_gemm_t<192, DLO_EPI_BIAS_GELU>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_BIAS_GELU * 3 + 2: return launch_gemm_t<256, DLO_EPI_BIAS_GELU>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_GATED_RESIDUAL * 3 + 0:
             return launch_gemm_t<128, DLO_EPI_GATED_RESIDUAL>(tmA, tmW, d, st, num_sms);
-        case DLO_EPI_GATED_RESIDUAL * 2 + 1:
+        case DLO_EPI_GATED_RESIDUAL * 3 + 1:
+            return launch_gemm_t<192, DLO_EPI_GATED_RESIDUAL>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_GATED_RESIDUAL * 3 + 2:
             return launch_gemm_t<256, DLO_EPI_GATED_RESIDUAL>(tmA, tmW, d, st, num_sms);
         default: return set_error(DLO_ERR_INVALID_ARG, "gemm: unknown epilogue %d", a.epilogue);
     }
