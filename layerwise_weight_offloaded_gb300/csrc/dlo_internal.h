@@ -82,7 +82,12 @@ struct GemmArgs {
     int gate_stride;
     int T;
     int* err;
+    const CUtensorMap* out_map = nullptr;  // from encode_gemm_out_map(out, ...), or null: encoded per launch
 };
+// Tensor map the GEMM epilogue writes through: bf16 [M, N] (DLO_EPI_BIAS,
+// DLO_EPI_BIAS_GELU) or the fp32 [M, N] residual stream it adds into
+// (DLO_EPI_GATED_RESIDUAL), in boxes of 32 rows x 64 bytes, 64-byte swizzle.
+int encode_gemm_out_map(CUtensorMap* map, void* out, int epilogue, uint64_t M, uint64_t N);
 // Tensor maps from encode_tmap_bf16: A over [M, K] with box rows 128; the two
 // W [N, K] maps from encode_gemm_w_maps (the kernel picks its tile width per
 // shape and loads the W tile as one 256-row box or two or three 64-row boxes).

@@ -85,6 +85,24 @@ int encode_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_
     return DLO_OK;
 }
 
+int encode_gemm_out_map(CUtensorMap* map, void* out, int epilogue, uint64_t M, uint64_t N) {
+    auto enc = tmap_encoder();
+    if (!enc) return set_error(DLO_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    const bool f32 = epilogue == DLO_EPI_GATED_RESIDUAL;
+    const uint64_t esz = f32 ? 4 : 2;
+    if (reinterpret_cast<uintptr_t>(out) % 16 || (N * esz) % 16)
+        return set_error(DLO_ERR_ALIGNMENT, "tensor map: output base or row pitch not 16-byte aligned");
+    cuuint64_t dims[2] = {N, M};
+    cuuint64_t strides[1] = {N * esz};
+    cuuint32_t box[2] = {f32 ? 16u : 32u, 32};  // 64-byte box rows either way
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(DLO_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (CUresult %d)", (int)r);
+    return DLO_OK;
+}
+
 int encode_gemm_w_maps(CUtensorMap* tmW, const void* W, uint64_t N, uint64_t K) {
     int rc = encode_tmap_bf16(&tmW[0], W, K, N, 64);
     return rc ? rc : encode_tmap_bf16(&tmW[1], W, K, N, 256);
@@ -133,7 +151,9 @@ struct BlockMaps {
     CUtensorMap qkv[2], proj[2], fc1[2], fc2[2];
 };
 struct ActMaps {
-    CUtensorMap u, o, g;
+    CUtensorMap u, o, g;        // GEMM A operands
+    CUtensorMap qkv_out, g_out;  // GEMM outputs (bf16)
+    CUtensorMap x_out;           // the residual stream the gated epilogues add into
 };
 
 struct ProfEvent {
@@ -179,6 +199,7 @@ struct dlo_handle {
     uint16_t *u = nullptr, *qkv = nullptr, *o = nullptr, *g = nullptr;
     int64_t act_rows = -1;  // rows the activation maps were encoded for
     std::vector<ActMaps> amaps;
+    const float* x_map_ptr = nullptr;  // x the amaps' x_out maps were encoded for (rows = act_rows)
     // host-buffer forward staging
     float* x_dev = nullptr;
     float* c_dev = nullptr;
@@ -311,9 +332,23 @@ int ensure_activations(dlo_handle* h, int R, int T) {
             if ((rc = encode_tmap_bf16(&h->amaps[b].u, h->u, sp.hidden, M, 128))) return rc;
             if ((rc = encode_tmap_bf16(&h->amaps[b].o, h->o, sp.hidden, M, 128))) return rc;
             if ((rc = encode_tmap_bf16(&h->amaps[b].g, h->g, sp.mlp_hidden, M, 128))) return rc;
+            if ((rc = encode_gemm_out_map(&h->amaps[b].qkv_out, h->qkv, DLO_EPI_BIAS, M, 3 * sp.hidden))) return rc;
+            if ((rc = encode_gemm_out_map(&h->amaps[b].g_out, h->g, DLO_EPI_BIAS_GELU, M, sp.mlp_hidden))) return rc;
         }
         h->act_rows = M;
+        h->x_map_ptr = nullptr;
     }
+    return DLO_OK;
+}
+
+// The residual stream's output maps, re-encoded when the caller's x changes.
+int ensure_x_maps(dlo_handle* h, float* x, int64_t M) {
+    if (x == h->x_map_ptr) return DLO_OK;
+    for (int b = 0; b < h->L; ++b) {
+        int rc = encode_gemm_out_map(&h->amaps[b].x_out, x, DLO_EPI_GATED_RESIDUAL, M, h->specs[b].hidden);
+        if (rc) return rc;
+    }
+    h->x_map_ptr = x;
     return DLO_OK;
 }
 
@@ -347,6 +382,7 @@ int run_block(dlo_handle* h, int b, int slot, float* x, const float* cond, int R
 
     e = prof_begin(h, DLO_K_GEMM_QKV, s);
     a.epilogue = DLO_EPI_BIAS; a.N = 3 * hd; a.K = hd; a.bias = w + of[DLO_P_QKV_B]; a.out = h->qkv; a.gate = nullptr;
+    a.out_map = &am.qkv_out;
     if ((rc = launch_gemm(am.u, bm.qkv, a, s, h->dev.num_sms))) return rc;
     prof_end(e, s);
 
@@ -356,7 +392,7 @@ int run_block(dlo_handle* h, int b, int slot, float* x, const float* cond, int R
 
     e = prof_begin(h, DLO_K_GEMM_PROJ, s);
     a.epilogue = DLO_EPI_GATED_RESIDUAL; a.N = hd; a.K = hd; a.bias = w + of[DLO_P_PROJ_B]; a.out = x;
-    a.gate = mod + 2 * hd; a.gate_stride = ms;
+    a.gate = mod + 2 * hd; a.gate_stride = ms; a.out_map = &am.x_out;
     if ((rc = launch_gemm(am.o, bm.proj, a, s, h->dev.num_sms))) return rc;
     prof_end(e, s);
 
@@ -366,12 +402,13 @@ int run_block(dlo_handle* h, int b, int slot, float* x, const float* cond, int R
 
     e = prof_begin(h, DLO_K_GEMM_FC1, s);
     a.epilogue = DLO_EPI_BIAS_GELU; a.N = m; a.K = hd; a.bias = w + of[DLO_P_FC1_B]; a.out = h->g; a.gate = nullptr;
+    a.out_map = &am.g_out;
     if ((rc = launch_gemm(am.u, bm.fc1, a, s, h->dev.num_sms))) return rc;
     prof_end(e, s);
 
     e = prof_begin(h, DLO_K_GEMM_FC2, s);
     a.epilogue = DLO_EPI_GATED_RESIDUAL; a.N = hd; a.K = m; a.bias = w + of[DLO_P_FC2_B]; a.out = x;
-    a.gate = mod + 5 * hd; a.gate_stride = ms;
+    a.gate = mod + 5 * hd; a.gate_stride = ms; a.out_map = &am.x_out;
     if ((rc = launch_gemm(am.g, bm.fc2, a, s, h->dev.num_sms))) return rc;
     prof_end(e, s);
 
@@ -568,6 +605,7 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int rc;
     if ((rc = ensure_activations(h, R, T))) return fail(h, rc);
+    if ((rc = ensure_x_maps(h, x, (int64_t)R * T))) return fail(h, rc);
     h->prof_used = 0;
     cudaError_t e;
 #define FWD_TRY(expr)                                            \

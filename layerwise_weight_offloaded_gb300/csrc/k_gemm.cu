@@ -16,8 +16,13 @@
 //   warps 2-9  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
 //              lanes 32*(w%4)..+31 = its 32 rows; warps 2-5 take the first
 //              half of the tile's columns, warps 6-9 the second), bias + GELU
-//              or gated residual, global stores.  Two accumulators alternate,
-//              so the epilogue of tile i overlaps the MMAs of tile i+1.
+//              or gate * (acc + bias), 32 columns at a time, staged in 2 KB
+//              shared-memory boxes and written by a TMA store (bf16 out) or a
+//              TMA add into
+//              the fp32 residual stream x (the read-modify-write happens at
+//              L2, so the epilogue never loads x).  Two accumulators
+//              alternate, so the epilogue of tile i overlaps the MMAs of tile
+//              i+1.
 // Tiles are walked M-fastest so CTAs running together share a W panel in L2.
 // Every wait is bounded (dlo_device.cuh); on expiry the kernel records an
 // error code, waits for its own copies and MMAs, frees TMEM and returns.
@@ -32,17 +37,27 @@ constexpr int kGemmThreads = 320;
 constexpr int kGemmEpiThreads = 256;
 constexpr unsigned kFullMask = 0xffffffffu;
 
-template <int BN>
+template <int BN, int EPI>
 struct GemmCfg {
     static_assert(BN == 128 || BN == 192 || BN == 256, "tile widths 128, 192, 256");
-    static constexpr int kStages = BN == 256 ? 4 : BN == 192 ? 5 : 6;
     static constexpr int kABytes = kGemmBM * kGemmBK * 2;
     static constexpr int kBBytes = BN * kGemmBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kWBox = BN == 256 ? 256 : 64;  // rows per W copy (the W map's box)
     static constexpr int kTmemCols = BN == 128 ? 256 : 512;  // two accumulators, power of two
+    // per epilogue warp: one 2 KB box of the output with 64-byte rows, staged
+    // for its TMA store (bf16: 32 rows x 32 columns) or TMA add (fp32: 32 rows x
+    // 16 columns, two per 32-column chunk)
+    static constexpr bool kF32Out = EPI == DLO_EPI_GATED_RESIDUAL;
+    static constexpr int kBoxCols = kF32Out ? 16 : 32;
+    static constexpr int kEpiBoxBytes = 2048;
+    static constexpr int kEpiBytes = 8 * kEpiBoxBytes;
     static constexpr int kBarBytes = 256;
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + kBarBytes;
+    static constexpr int kFixedBytes = kEpiBytes + 1024 + kBarBytes;  // + alignment slack
+    static constexpr int kStagesFit = (227 * 1024 - kFixedBytes) / kStageBytes;
+    static constexpr int kStages = kStagesFit < 6 ? kStagesFit : 6;
+    static constexpr int kSmemBytes = kStages * kStageBytes + kFixedBytes;
+    static_assert(kStages >= 3, "pipeline depth");
     static_assert(2 * BN <= kTmemCols && kTmemCols <= 512, "TMEM holds 512 columns");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
@@ -50,7 +65,6 @@ struct GemmCfg {
 struct GemmDevArgs {
     int M, N, K;
     const uint16_t* bias;
-    void* out;
     const float* gate;
     int gate_stride;
     int T;
@@ -72,54 +86,68 @@ __device__ __forceinline__ float gelu_tanh_f(float v) {
     return v * rcp_approx(1.0f + e);
 }
 
-// Epilogue of one row segment of 32 accumulator columns starting at col0.
+// Epilogue arithmetic on one row segment of 32 accumulator columns starting at
+// col0 (columns at or past N are left as they are: the TMA store drops them).
+// bias / bias + GELU give the output value; the gated residual gives the
+// increment gate * (acc + bias) that the TMA add applies to x.
 template <int EPI>
-__device__ __forceinline__ void epilogue_32(const GemmDevArgs& p, int row, int col0, const float* acc) {
+__device__ __forceinline__ void epilogue_32(const GemmDevArgs& p, const float* gate_row, int col0, float* v) {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         const int col = col0 + 8 * g;
         if (col >= p.N) break;
         const uint4 bw = __ldg(reinterpret_cast<const uint4*>(p.bias + col));
-        float b[8] = {bf16_lo(bw.x), bf16_hi(bw.x), bf16_lo(bw.y), bf16_hi(bw.y),
-                      bf16_lo(bw.z), bf16_hi(bw.z), bf16_lo(bw.w), bf16_hi(bw.w)};
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = acc[8 * g + i] + b[i];
+        const float b[8] = {bf16_lo(bw.x), bf16_hi(bw.x), bf16_lo(bw.y), bf16_hi(bw.y),
+                            bf16_lo(bw.z), bf16_hi(bw.z), bf16_lo(bw.w), bf16_hi(bw.w)};
         if constexpr (EPI == DLO_EPI_GATED_RESIDUAL) {
-            float* x = reinterpret_cast<float*>(p.out) + (size_t)row * p.N + col;
-            const float* gt = p.gate + (size_t)(row / p.T) * p.gate_stride + col;
-            const float4 g0 = *reinterpret_cast<const float4*>(gt);
-            const float4 g1 = *reinterpret_cast<const float4*>(gt + 4);
-            float4 x0 = *reinterpret_cast<float4*>(x);
-            float4 x1 = *reinterpret_cast<float4*>(x + 4);
-            x0.x += g0.x * v[0]; x0.y += g0.y * v[1]; x0.z += g0.z * v[2]; x0.w += g0.w * v[3];
-            x1.x += g1.x * v[4]; x1.y += g1.y * v[5]; x1.z += g1.z * v[6]; x1.w += g1.w * v[7];
-            *reinterpret_cast<float4*>(x) = x0;
-            *reinterpret_cast<float4*>(x + 4) = x1;
-        } else {
-            if constexpr (EPI == DLO_EPI_BIAS_GELU) {
+            const float4 g0 = __ldg(reinterpret_cast<const float4*>(gate_row + col));
+            const float4 g1 = __ldg(reinterpret_cast<const float4*>(gate_row + col + 4));
+            const float gt[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = gelu_tanh_f(v[i]);
+            for (int i = 0; i < 8; ++i) v[8 * g + i] = gt[i] * (v[8 * g + i] + b[i]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[8 * g + i] += b[i];
+                if constexpr (EPI == DLO_EPI_BIAS_GELU) v[8 * g + i] = gelu_tanh_f(v[8 * g + i]);
             }
-            uint4 o;
-            o.x = pack_bf16x2(v[0], v[1]);
-            o.y = pack_bf16x2(v[2], v[3]);
-            o.z = pack_bf16x2(v[4], v[5]);
-            o.w = pack_bf16x2(v[6], v[7]);
-            *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + (size_t)row * p.N + col) = o;
         }
+    }
+}
+
+// Writes a thread's values (its row r of the warp's 32-row box: 16 fp32 or 32
+// bf16 = 64 bytes) into the staging box in the layout of the output map's
+// 64-byte swizzle: 16-byte chunk j of row r at r * 64 + ((j ^ ((r / 2) % 4)) * 16).
+template <bool F32>
+__device__ __forceinline__ void stage_row(uint8_t* box, int r, const float* v) {
+    uint8_t* row = box + r * 64;
+    const int sw = (r >> 1) & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 w;
+        if constexpr (F32) {
+            w = make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                           __float_as_uint(v[4 * j + 3]));
+        } else {
+            w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+            w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+            w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+            w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+        }
+        *reinterpret_cast<uint4*>(row + ((j ^ sw) << 4)) = w;
     }
 }
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_bf16_tcgen05(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                      const GemmDevArgs p) {
-    using Cfg = GemmCfg<BN>;
+                      const __grid_constant__ CUtensorMap tmOut, const GemmDevArgs p) {
+    using Cfg = GemmCfg<BN, EPI>;
     constexpr int S = Cfg::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * Cfg::kStageBytes);
+    uint8_t* epi_boxes = smem + S * Cfg::kStageBytes;  // 1024-byte aligned: kStageBytes is
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi_boxes + Cfg::kEpiBytes);
     uint64_t* empty = full + S;
     uint64_t* acc_full = empty + S;
     uint64_t* acc_empty = acc_full + 2;
@@ -146,6 +174,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_mbarrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmOut);
     }
     if (warp == 1) tmem_alloc(tmem_slot, Cfg::kTmemCols);
     tc_fence_before();
@@ -235,7 +264,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // ---------------- epilogue warps 2..9
         const int quarter = warp & 3;
         const int c_begin = warp < 6 ? 0 : BN / 2;  // this warp's half of the tile's columns
-        const int row_in_tile = quarter * 32 + lane;
+        uint8_t* box = epi_boxes + (warp - 2) * Cfg::kEpiBoxBytes;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -245,19 +274,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!__all_sync(kFullMask, mbar_wait_bounded(&acc_full[acc], acc_phase, p.err, KERR_GEMM_EPILOGUE)))
                 break;
             tc_fence_after();
-            const int row = m0 + row_in_tile;
+            const int row0 = m0 + quarter * 32;  // first row of this warp's 32-row box
+            const float* gate_row = nullptr;
+            if constexpr (EPI == DLO_EPI_GATED_RESIDUAL) {
+                const int row = min(row0 + lane, p.M - 1);  // rows past M are computed, never stored
+                gate_row = p.gate + (size_t)(row / p.T) * p.gate_stride;
+            }
             const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
-            for (int c = c_begin; c < c_begin + BN / 2; c += 32) {
+            for (int c = c_begin; c < c_begin + BN / 2 && n0 + c < p.N; c += 32) {
                 float v[32];
                 tmem_ld_32x32b_x32(taddr + (uint32_t)c, v);
-                if (row < p.M && n0 + c < p.N) epilogue_32<EPI>(p, row, n0 + c, v);
+                epilogue_32<EPI>(p, gate_row, n0 + c, v);
+#pragma unroll
+                for (int bc = 0; bc < 32; bc += Cfg::kBoxCols) {
+                    // the previous box must have been read out before it is rewritten
+                    if (lane == 0) bulk_wait_group_read0();
+                    __syncwarp();
+                    stage_row<Cfg::kF32Out>(box, lane, v + bc);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (Cfg::kF32Out)
+                            tma_reduce_add_2d(&tmOut, box, n0 + c + bc, row0);
+                        else
+                            tma_store_2d(&tmOut, box, n0 + c + bc, row0);
+                        bulk_commit_group();
+                    }
+                }
             }
             tc_fence_before();
             mbar_arrive(&acc_empty[acc]);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+        // the stores and adds issued here complete before the CTA exits
+        if (lane == 0) bulk_wait_group0();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -295,9 +348,9 @@ int gemm_block_n(int M, int N, int num_sms) {
 }
 
 template <int BN, int EPI>
-static int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmW, const GemmDevArgs& d, cudaStream_t st,
-                         int num_sms) {
-    using Cfg = GemmCfg<BN>;
+static int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmW, const CUtensorMap& tmOut,
+                         const GemmDevArgs& d, cudaStream_t st, int num_sms) {
+    using Cfg = GemmCfg<BN, EPI>;
     static bool configured[64] = {};
     int dev = 0;
     DLO_CUDA_TRY(cudaGetDevice(&dev));
@@ -309,7 +362,8 @@ static int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmW, const G
     }
     const int tiles = ((d.M + kGemmBM - 1) / kGemmBM) * ((d.N + BN - 1) / BN);
     const int grid = tiles < num_sms ? tiles : num_sms;
-    DLO_CUDA_TRY(launch_pdl(gemm_bf16_tcgen05<BN, EPI>, dim3(grid), dim3(kGemmThreads), Cfg::kSmemBytes, st, tmA, tmW, d));
+    DLO_CUDA_TRY(launch_pdl(gemm_bf16_tcgen05<BN, EPI>, dim3(grid), dim3(kGemmThreads), Cfg::kSmemBytes, st, tmA, tmW,
+                            tmOut, d));
     DLO_CUDA_TRY(cudaGetLastError());
     return DLO_OK;
 }
@@ -320,23 +374,30 @@ int launch_gemm(const CUtensorMap& tmA, const CUtensorMap* tmWs, const GemmArgs&
     if (!a.bias || !a.out || !a.err) return set_error(DLO_ERR_INVALID_ARG, "gemm: null pointer");
     if (a.epilogue == DLO_EPI_GATED_RESIDUAL && (!a.gate || a.T <= 0 || a.gate_stride % 4))
         return set_error(DLO_ERR_INVALID_ARG, "gemm: gated residual needs gate, T > 0, gate_stride % 4 == 0");
-    GemmDevArgs d{a.M, a.N, a.K, a.bias, a.out, a.gate, a.gate_stride, a.T, a.err};
+    GemmDevArgs d{a.M, a.N, a.K, a.bias, a.gate, a.gate_stride, a.T, a.err};
+    CUtensorMap out_local;
+    const CUtensorMap* tmOut = a.out_map;
+    if (!tmOut) {
+        int rc = encode_gemm_out_map(&out_local, a.out, a.epilogue, (uint64_t)a.M, (uint64_t)a.N);
+        if (rc) return rc;
+        tmOut = &out_local;
+    }
     const int bn = gemm_block_n(a.M, a.N, num_sms);
     const CUtensorMap& tmW = tmWs[bn == 256 ? 1 : 0];
     const int wi = bn == 128 ? 0 : bn == 192 ? 1 : 2;
     switch (a.epilogue * 3 + wi) {
-        case DLO_EPI_BIAS * 3 + 0: return launch_gemm_t<128, DLO_EPI_BIAS>(tmA, tmW, d, st, num_sms);
-        case DLO_EPI_BIAS * 3 + 1: return launch_gemm_t<192, DLO_EPI_BIAS>(tmA, tmW, d, st, num_sms);
-        case DLO_EPI_BIAS * 3 + 2: return launch_gemm_t<256, DLO_EPI_BIAS>(tmA, tmW, d, st, num_sms);
-        case DLO_EPI_BIAS_GELU * 3 + 0: return launch_gemm_t<128, DLO_EPI_BIAS_GELU>(tmA, tmW, d, st, num_sms);
-        case DLO_EPI_BIAS_GELU * 3 + 1: return launch_gemm_t<192, DLO_EPI_BIAS_GELU>(tmA, tmW, d, st, num_sms);
-        case DLO_EPI_BIAS_GELU * 3 + 2: return launch_gemm_t<256, DLO_EPI_BIAS_GELU>(tmA, tmW, d, st, num_sms);
+        case DLO_EPI_BIAS * 3 + 0: return launch_gemm_t<128, DLO_EPI_BIAS>(tmA, tmW, *tmOut, d, st, num_sms);
+        case DLO_EPI_BIAS * 3 + 1: return launch_gemm_t<192, DLO_EPI_BIAS>(tmA, tmW, *tmOut, d, st, num_sms);
+        case DLO_EPI_BIAS * 3 + 2: return launch_gemm_t<256, DLO_EPI_BIAS>(tmA, tmW, *tmOut, d, st, num_sms);
+        case DLO_EPI_BIAS_GELU * 3 + 0: return launch_gemm_t<128, DLO_EPI_BIAS_GELU>(tmA, tmW, *tmOut, d, st, num_sms);
+        case DLO_EPI_BIAS_GELU * 3 + 1: return launch_gemm_t<192, DLO_EPI_BIAS_GELU>(tmA, tmW, *tmOut, d, st, num_sms);
+        case DLO_EPI_BIAS_GELU * 3 + 2: return launch_gemm_t<256, DLO_EPI_BIAS_GELU>(tmA, tmW, *tmOut, d, st, num_sms);
         case DLO_EPI_GATED_RESIDUAL * 3 + 0:
-            return launch_gemm_t<128, DLO_EPI_GATED_RESIDUAL>(tmA, tmW, d, st, num_sms);
+            return launch_gemm_t<128, DLO_EPI_GATED_RESIDUAL>(tmA, tmW, *tmOut, d, st, num_sms);
         case DLO_EPI_GATED_RESIDUAL * 3 + 1:
-            return launch_gemm_t<192, DLO_EPI_GATED_RESIDUAL>(tmA, tmW, d, st, num_sms);
+            return launch_gemm_t<192, DLO_EPI_GATED_RESIDUAL>(tmA, tmW, *tmOut, d, st, num_sms);
         case DLO_EPI_GATED_RESIDUAL * 3 + 2:
-            return launch_gemm_t<256, DLO_EPI_GATED_RESIDUAL>(tmA, tmW, d, st, num_sms);
+            return launch_gemm_t<256, DLO_EPI_GATED_RESIDUAL>(tmA, tmW, *tmOut, d, st, num_sms);
         default: return set_error(DLO_ERR_INVALID_ARG, "gemm: unknown epilogue %d", a.epilogue);
     }
 }

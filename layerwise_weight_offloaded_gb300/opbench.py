@@ -1,0 +1,115 @@
+"""Single-kernel micro-benchmark through the single-op C-ABI entry points.
+
+    python -m layerwise_weight_offloaded_gb300.opbench <case> [--reps N] [--warmup W]
+
+Runs one kernel of the DiT block on random device inputs of a named workload
+shape and prints its CUDA-event time and rate.  This is the driver the ncu
+summaries under profiles/ are captured from (`ncu -k regex:<kernel> -s W -c 1`
+skips the warm-up launches and captures the first timed one).
+
+Cases (M = R*T rows; weights [N, K] row-major):
+    t2i-attention     R=1 T=4096  H=24 d=64          (T2I-shaped DiT)
+    deep-attention    R=1 T=8192  H=24 d=128         (Deep DiT)
+    video-attention   R=1 T=16384 H=40 d=128         (Video-shaped DiT)
+    t2i-qkv / t2i-proj / t2i-fc1 / t2i-fc2           M=4096, h=1536, m=6144
+    deep-qkv / deep-proj / deep-fc1 / deep-fc2       M=8192, h=3072, m=12288
+    t2i-ln            LayerNorm+modulate, M=4096 h=1536
+    t2i-adaln         adaLN GEMV, R=1, C=256, N=6h=9216
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+import torch
+
+from . import _binding as B
+
+_LINEAR = {
+    # name: (M, N, K, epilogue)
+    "t2i-qkv": (4096, 3 * 1536, 1536, B.DLO_EPI_BIAS),
+    "t2i-proj": (4096, 1536, 1536, B.DLO_EPI_GATED_RESIDUAL),
+    "t2i-fc1": (4096, 6144, 1536, B.DLO_EPI_BIAS_GELU),
+    "t2i-fc2": (4096, 1536, 6144, B.DLO_EPI_GATED_RESIDUAL),
+    "deep-qkv": (8192, 3 * 3072, 3072, B.DLO_EPI_BIAS),
+    "deep-proj": (8192, 3072, 3072, B.DLO_EPI_GATED_RESIDUAL),
+    "deep-fc1": (8192, 12288, 3072, B.DLO_EPI_BIAS_GELU),
+    "deep-fc2": (8192, 3072, 12288, B.DLO_EPI_GATED_RESIDUAL),
+}
+_ATTENTION = {
+    # name: (R, T, H, d)
+    "t2i-attention": (1, 4096, 24, 64),
+    "deep-attention": (1, 8192, 24, 128),
+    "video-attention": (1, 16384, 40, 128),
+}
+CASES = tuple(_ATTENTION) + tuple(_LINEAR) + ("t2i-ln", "t2i-adaln")
+
+
+def _bf16_bits(t: torch.Tensor) -> torch.Tensor:
+    return t.to(torch.bfloat16).view(torch.int16)
+
+
+def make_case(name: str, gen: torch.Generator):
+    """Returns (launch, work, unit): launch() enqueues one kernel on the current
+    stream; work is the algorithmic FLOPs or bytes of one launch."""
+    dev = "cuda"
+    if name in _ATTENTION:
+        R, T, H, d = _ATTENTION[name]
+        qkv = _bf16_bits(torch.randn(R * T, 3 * H * d, device=dev, generator=gen))
+        o = torch.empty(R * T, H * d, dtype=torch.int16, device=dev)
+        return (lambda: B.dlo_op_attention(qkv, R, T, H, d, o)), 4.0 * R * T * T * H * d, "TFLOP/s"
+    if name in _LINEAR:
+        M, N, K, epi = _LINEAR[name]
+        A = _bf16_bits(torch.randn(M, K, device=dev, generator=gen))
+        W = _bf16_bits(torch.randn(N, K, device=dev, generator=gen) * 0.02)
+        bias = _bf16_bits(torch.randn(N, device=dev, generator=gen) * 0.02)
+        if epi == B.DLO_EPI_GATED_RESIDUAL:
+            out = torch.randn(M, N, device=dev, generator=gen)
+        else:
+            out = torch.empty(M, N, dtype=torch.int16, device=dev)
+        gate = torch.rand(1, N, device=dev, generator=gen)
+        return ((lambda: B.dlo_op_linear(epi, A, W, bias, M, N, K, out, gate, N, M)),
+                2.0 * M * N * K, "TFLOP/s")
+    if name == "t2i-ln":
+        M, h = 4096, 1536
+        x = torch.randn(M, h, device=dev, generator=gen)
+        mod = torch.randn(1, 6 * h, device=dev, generator=gen)
+        u = torch.empty(M, h, dtype=torch.int16, device=dev)
+        return (lambda: B.dlo_op_ln_modulate(x, mod, mod[:, h:], 6 * h, 1, M, h, u)), M * h * 6.0, "GB/s"
+    if name == "t2i-adaln":
+        h, C = 1536, 256
+        W = _bf16_bits(torch.randn(6 * h, C, device=dev, generator=gen) * 0.02)
+        b = _bf16_bits(torch.zeros(6 * h, device=dev))
+        c = torch.randn(1, C, device=dev, generator=gen)
+        mod = torch.empty(1, 6 * h, device=dev)
+        return (lambda: B.dlo_op_adaln(W, b, c, 1, C, 6 * h, mod)), 6.0 * h * C * 2, "GB/s"
+    raise SystemExit(f"unknown case {name!r}; known: {', '.join(CASES)}")
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("case", choices=CASES)
+    ap.add_argument("--warmup", type=int, default=3, help="untimed launches first")
+    ap.add_argument("--reps", type=int, default=1, help="timed launches (reported: their mean)")
+    args = ap.parse_args(argv)
+    if not torch.cuda.is_available():
+        raise SystemExit("opbench needs a CUDA device")
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    launch, work, unit = make_case(args.case, gen)
+    for _ in range(args.warmup):
+        launch()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.reps):
+        launch()
+    e1.record()
+    torch.cuda.synchronize()
+    B.dlo_op_check()
+    us = e0.elapsed_time(e1) * 1e3 / args.reps
+    rate = work / us / (1e6 if unit == "TFLOP/s" else 1e3)
+    print(f"{args.case}: {us:.1f} us per launch, {rate:.0f} {unit}")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
