@@ -18,8 +18,9 @@ Cases (M = R*T rows; weights [N, K] row-major):
     t2i-qkv / t2i-proj / t2i-fc1 / t2i-fc2           M=4096, h=1536, m=6144
     deep-qkv / deep-proj / deep-fc1 / deep-fc2       M=8192, h=3072, m=12288
     large-fc2                                        M=16384, h=8192, m=32768
-    t2i-ln            LayerNorm+modulate, M=4096 h=1536
-    t2i-adaln         adaLN GEMV, R=1, C=256, N=6h=9216
+    t2i-ln / video-ln / large-ln       LayerNorm+modulate, R*T x h = 4096x1536 /
+                                       16384x5120 / 4x4096 x 8192
+    t2i-adaln / large-adaln            adaLN GEMV, C=256: R=1, h=1536 / R=4, h=8192
 """
 from __future__ import annotations
 
@@ -48,7 +49,18 @@ _ATTENTION = {
     "deep-attention": (1, 8192, 24, 128),
     "video-attention": (1, 16384, 40, 128),
 }
-CASES = tuple(_ATTENTION) + tuple(_LINEAR) + ("t2i-ln", "t2i-adaln")
+_LN = {
+    # name: (R, T, h)
+    "t2i-ln": (1, 4096, 1536),
+    "video-ln": (1, 16384, 5120),
+    "large-ln": (4, 4096, 8192),
+}
+_ADALN = {
+    # name: (R, h, C)
+    "t2i-adaln": (1, 1536, 256),
+    "large-adaln": (4, 8192, 256),
+}
+CASES = tuple(_ATTENTION) + tuple(_LINEAR) + tuple(_LN) + tuple(_ADALN)
 
 
 def _bf16_bits(t: torch.Tensor) -> torch.Tensor:
@@ -76,19 +88,21 @@ def make_case(name: str, gen: torch.Generator):
         gate = torch.rand(1, N, device=dev, generator=gen)
         return ((lambda: B.dlo_op_linear(epi, A, W, bias, M, N, K, out, gate, N, M)),
                 2.0 * M * N * K, "TFLOP/s")
-    if name == "t2i-ln":
-        M, h = 4096, 1536
+    if name in _LN:
+        R, T, h = _LN[name]
+        M = R * T
         x = torch.randn(M, h, device=dev, generator=gen)
-        mod = torch.randn(1, 6 * h, device=dev, generator=gen)
+        mod = torch.randn(R, 6 * h, device=dev, generator=gen)
         u = torch.empty(M, h, dtype=torch.int16, device=dev)
-        return (lambda: B.dlo_op_ln_modulate(x, mod, mod[:, h:], 6 * h, 1, M, h, u)), M * h * 6.0, "GB/s"
-    if name == "t2i-adaln":
-        h, C = 1536, 256
+        return ((lambda: B.dlo_op_ln_modulate(x, mod, mod[:, h:], 6 * h, R, T, h, u)),
+                M * h * 6.0 + R * h * 8.0, "GB/s")
+    if name in _ADALN:
+        R, h, C = _ADALN[name]
         W = _bf16_bits(torch.randn(6 * h, C, device=dev, generator=gen) * 0.02)
         b = _bf16_bits(torch.zeros(6 * h, device=dev))
-        c = torch.randn(1, C, device=dev, generator=gen)
-        mod = torch.empty(1, 6 * h, device=dev)
-        return (lambda: B.dlo_op_adaln(W, b, c, 1, C, 6 * h, mod)), 6.0 * h * C * 2, "GB/s"
+        c = torch.randn(R, C, device=dev, generator=gen)
+        mod = torch.empty(R, 6 * h, device=dev)
+        return (lambda: B.dlo_op_adaln(W, b, c, R, C, 6 * h, mod)), 6.0 * h * C * 2 + R * 6 * h * 4, "GB/s"
     raise SystemExit(f"unknown case {name!r}; known: {', '.join(CASES)}")
 
 
