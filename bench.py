@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--no-profile", action="store_true", help="no per-kernel events in the timed region")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--clock-interval-ms", type=int, default=200, help="nvidia-smi sampling period; 0 = no sampling")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="requests sharing each streamed block (default: the workload's own R); the fill per "
+                         "block is fixed, so this sweeps how it is amortised")
     return ap.parse_args()
 
 
@@ -233,6 +236,9 @@ def main():
     args = parse()
     import synthetic
     cfg = synthetic.get_config(args.workload)
+    if args.requests > 0:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, requests=args.requests)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -204,6 +204,19 @@ int dlo_create(const dlo_block_spec* specs, int32_t num_blocks, int32_t dp_size,
 int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t num_requests,
                 int32_t tokens_per_request, dlo_stream_t stream);
 
+/* A denoising loop's worth of forwards: n_steps >= 1 calls of dlo_forward
+ * on the same x, step k conditioned on cond_steps + k*num_requests*cond_dim
+ * (device fp32 [n_steps, R, cond_dim]).  x carries each step's output into
+ * the next; a sampler's latent update between steps is outside this path.
+ * The write-up runs the layerwise pipeline once per denoising step (section 3,
+ * and the 35- to 50-step workloads of its results section); with
+ * DLO_PREFETCH_NEXT each step's last block overlaps the fill of the next
+ * step's block 0, so only the first step pays an exposed fill.  Same
+ * ordering, ownership and errors as dlo_forward; on an error, the steps
+ * already enqueued stay enqueued. */
+int dlo_forward_steps(dlo_handle* h, float* x, const float* cond_steps, int32_t n_steps,
+                      int32_t num_requests, int32_t tokens_per_request, dlo_stream_t stream);
+
 /* Same forward from HOST buffers: copies x_host [R,T,hidden] and cond_host
  * [R,cond_dim] to device staging buffers owned by the handle, runs
  * dlo_forward on `stream`, copies the result back into x_host and waits for

@@ -44,7 +44,7 @@ EXPORTED = (
     "dlo_last_error", "dlo_status_string", "dlo_create", "dlo_forward", "dlo_forward_host", "dlo_synchronize",
     "dlo_get_stats", "dlo_get_kernel_times", "dlo_debug_fill_and_read", "dlo_destroy", "dlo_op_adaln",
     "dlo_op_ln_modulate", "dlo_op_linear", "dlo_op_attention", "dlo_op_shard_gather", "dlo_op_check",
-    "dlo_op_linear_noalloc",
+    "dlo_op_linear_noalloc", "dlo_forward_steps",
 )
 
 
@@ -86,6 +86,7 @@ _SIGS = {
     "dlo_create": [ctypes.POINTER(dlo_block_spec), _c_i32, _c_i32, ctypes.POINTER(_c_p), _c_u32, ctypes.POINTER(_c_p)],
     "dlo_forward": [_c_p, _c_p, _c_p, _c_i32, _c_i32, _c_p],
     "dlo_forward_host": [_c_p, _c_p, _c_p, _c_i32, _c_i32, _c_p],
+    "dlo_forward_steps": [_c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_p],
     "dlo_synchronize": [_c_p, _c_i32],
     "dlo_get_stats": [_c_p, ctypes.POINTER(dlo_stats)],
     "dlo_get_kernel_times": [_c_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_c_i64)],
@@ -223,6 +224,13 @@ def dlo_forward_host(handle: int, x_host, cond_host, num_requests: int, tokens_p
                      stream=None) -> None:
     _check(lib().dlo_forward_host(handle, _ptr(x_host), _ptr(cond_host), num_requests, tokens_per_request,
                                   _stream(stream)))
+
+
+def dlo_forward_steps(handle: int, x, cond_steps, n_steps: int, num_requests: int, tokens_per_request: int,
+                      stream=None) -> None:
+    """n_steps forwards on x, step k conditioned on cond_steps[k] ([n_steps, R, cond_dim])."""
+    _check(lib().dlo_forward_steps(handle, _ptr(x), _ptr(cond_steps), n_steps, num_requests, tokens_per_request,
+                                   _stream(stream)))
 
 
 def dlo_synchronize(handle: int, timeout_ms: int = -1) -> None:

@@ -675,6 +675,19 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
     return DLO_OK;
 }
 
+int dlo_forward_steps(dlo_handle* h, float* x, const float* cond_steps, int32_t n_steps, int32_t R, int32_t T,
+                      dlo_stream_t stream) {
+    if (!h) return set_error(DLO_ERR_INVALID_ARG, "forward_steps: null handle");
+    if (n_steps < 1) return set_error(DLO_ERR_INVALID_ARG, "forward_steps: n_steps must be >= 1");
+    if (!cond_steps) return set_error(DLO_ERR_INVALID_ARG, "forward_steps: null cond_steps");
+    const int64_t per_step = (int64_t)std::max(R, 0) * h->specs[0].cond_dim;
+    for (int32_t k = 0; k < n_steps; ++k) {
+        int rc = dlo_forward(h, x, cond_steps + (size_t)k * per_step, R, T, stream);
+        if (rc) return rc;
+    }
+    return DLO_OK;
+}
+
 int dlo_forward_host(dlo_handle* h, float* x_host, const float* cond_host, int32_t R, int32_t T,
                      dlo_stream_t stream) {
     if (!h) return set_error(DLO_ERR_INVALID_ARG, "forward_host: null handle");

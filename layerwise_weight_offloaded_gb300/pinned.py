@@ -49,7 +49,7 @@ class PinnedShards:
                 shards = [buf[r * S:(r + 1) * S] for r in range(dp_size)]
             else:
                 shards = [torch.empty(S, dtype=torch.int16, pin_memory=True) for _ in range(dp_size)]
-            params = [np.ascontiguousarray(param_source(b, i, shape), dtype=np.uint16)
+            params = [np.ascontiguousarray(param_source(b, i, shape), dtype=np.uint16).reshape(-1)
                       for i, shape in enumerate(param_shapes(sp))]
             for p, shape in zip(params, param_shapes(sp)):
                 if p.size != int(np.prod(shape)):
@@ -66,3 +66,50 @@ class PinnedShards:
 
     def nbytes(self) -> int:
         return sum(s.numel() * 2 for blk in self.shards for s in blk)
+
+
+def block_flat_offsets(specs: Sequence) -> list[int]:
+    """Element offset of each block's flat buffer inside a flat weight file
+    holding the blocks back to back (block b's buffer is its parameters in
+    the DLO_P_* order, as dlo_param_table lays them out)."""
+    offs, at = [], 0
+    for sp in specs:
+        offs.append(at)
+        at += B.dlo_block_numel(B._spec(sp))
+    return offs
+
+
+def pack_from_flat_file(path: str, specs: Sequence, dp_size: int, contiguous: bool = False) -> "PinnedShards":
+    """Pinned shards packed straight from a memory-mapped flat bf16 weight file.
+
+    Section 1 of "vLLM-Omni 发布 Distributed Layerwise Offload…" builds the
+    model on the meta device and loads weights through mmap, so the process
+    never holds a private copy of the full checkpoint; section 2 then keeps
+    only each rank's shard pinned.  Here the file holds every block's flat
+    buffer back to back (block_flat_offsets); each block is packed from the
+    mapped pages into its pinned shards and the mapping is dropped before
+    returning.  The returned object carries ``mapped_bytes`` and
+    ``rss_high_water_kb`` (the process's peak resident set after packing).
+    """
+    import resource
+
+    specs = [B._spec(s) for s in specs]
+    offs = block_flat_offsets(specs)
+    total = offs[-1] + B.dlo_block_numel(specs[-1]) if specs else 0
+    flat = np.memmap(path, dtype=np.uint16, mode="r")
+    try:
+        if flat.size < total:
+            raise ValueError(f"{path}: {flat.size} bf16 elements, the blocks need {total}")
+
+        def source(b, i, shape):
+            p_off, p_num = B.dlo_param_table(specs[b])
+            start = offs[b] + p_off[i]
+            return flat[start:start + p_num[i]]
+
+        ps = PinnedShards(specs, dp_size, source, contiguous=contiguous)
+    finally:
+        mapped = flat.size * 2
+        del flat  # unmaps the file
+    ps.mapped_bytes = mapped
+    ps.rss_high_water_kb = resource.getrusage(resource.RUSAGE_SELF).ru_maxrss
+    return ps

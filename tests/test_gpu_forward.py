@@ -9,6 +9,7 @@ import torch
 import layerwise_weight_offloaded_gb300 as dlo
 import synthetic
 from layerwise_weight_offloaded_gb300.pinned import PinnedShards
+from layerwise_weight_offloaded_gb300.pinned import param_shapes as pinned_param_shapes
 from oracle import dit
 
 from _workload import assert_close_rel_max, oracle_params, param_source, spec_tuple, zero_gates
@@ -148,6 +149,74 @@ def test_prefetch_next_call_bit_exact(L):
     finally:
         plain.close()
         pre.close()
+
+
+def test_forward_steps_equals_sequential_forwards():
+    """dlo_forward_steps over n steps (each with its own cond) gives bit for bit
+    what n dlo_forward calls give, with and without cross-call prefetch."""
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * 3
+    R, T, n = 2, 96, 4
+    x, _ = inputs((R, T, cfg.hidden, cfg.cond_dim), 40)
+    conds = np.stack([synthetic.cond(41 + k, R, cfg.cond_dim) for k in range(n)])
+    ref = Run(specs, 2, 8, dlo.DLO_FILL_MEMCPY)
+    try:
+        want = x
+        for k in range(n):
+            want = ref.forward(want, conds[k])
+    finally:
+        ref.close()
+    for flags in (dlo.DLO_FILL_MEMCPY, dlo.DLO_FILL_MEMCPY | dlo.DLO_PREFETCH_NEXT):
+        run = Run(specs, 2, 8, flags)
+        try:
+            xd = torch.from_numpy(x).cuda()
+            cd = torch.from_numpy(conds).cuda()
+            dlo.dlo_forward_steps(run.h, xd, cd, n, R, T, torch.cuda.current_stream())
+            dlo.dlo_synchronize(run.h, 120000)
+            got = xd.cpu().numpy()
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), flags
+            assert dlo.dlo_get_stats(run.h)["forwards"] == n
+        finally:
+            run.close()
+    with pytest.raises(dlo.DloError):
+        dlo.dlo_forward_steps(0, 0, 0, 1, 1, 1)
+
+
+def test_pack_from_mmapped_flat_file(tmp_path):
+    """Shards packed from a memory-mapped flat weight file equal shards packed
+    from the parameter arrays, bit for bit, and stream the same forward."""
+    from layerwise_weight_offloaded_gb300.pinned import block_flat_offsets, pack_from_flat_file
+
+    specs = [(256, 4, 1024, 256), (256, 2, 512, 256), (256, 4, 768, 256)]
+    src = param_source(3)
+    path = tmp_path / "blocks.bf16"
+    with open(path, "wb") as f:
+        for b, sp in enumerate(specs):
+            for i, shape in enumerate(pinned_param_shapes(sp)):
+                np.ascontiguousarray(src(b, i, shape), dtype=np.uint16).tofile(f)
+    offs = block_flat_offsets(specs)
+    assert offs[1] == dlo.dlo_block_numel(specs[0])
+    assert path.stat().st_size == 2 * (offs[-1] + dlo.dlo_block_numel(specs[-1]))
+
+    ps = pack_from_flat_file(str(path), specs, 3)
+    ref = PinnedShards(specs, 3, src)
+    for b in range(len(specs)):
+        for r in range(3):
+            assert np.array_equal(ps.shard_numpy(b, r), ref.shard_numpy(b, r)), (b, r)
+    assert ps.mapped_bytes == path.stat().st_size and ps.rss_high_water_kb > 0
+
+    x, c = inputs((2, 64, 256, 256), 13)
+    outs = []
+    for shards in (ps, ref):
+        h = dlo.dlo_create(specs, 3, shards.ptrs, dlo.DLO_FILL_MEMCPY)
+        try:
+            xd, cd = torch.from_numpy(x).cuda(), torch.from_numpy(c).cuda()
+            dlo.dlo_forward(h, xd, cd, 2, 64, torch.cuda.current_stream())
+            dlo.dlo_synchronize(h, 120000)
+            outs.append(xd.cpu().numpy())
+        finally:
+            dlo.dlo_destroy(h)
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
 
 
 def test_zero_gates_identity_bit_exact():
