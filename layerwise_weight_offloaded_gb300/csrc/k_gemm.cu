@@ -23,9 +23,13 @@
 //              L2, so the epilogue never loads x).  Two accumulators
 //              alternate, so the epilogue of tile i overlaps the MMAs of tile
 //              i+1.
-// Tiles are walked M-fastest so CTAs running together share a W panel in L2.
+// Tiles are walked in groups of m-tiles (tile_coords) so the CTAs running
+// together share both A and W panels in L2.
 // Every wait is bounded (dlo_device.cuh); on expiry the kernel records an
 // error code, waits for its own copies and MMAs, frees TMEM and returns.
+#include <algorithm>
+#include <cmath>
+
 #include "dlo_device.cuh"
 #include "dlo_internal.h"
 
@@ -69,7 +73,24 @@ struct GemmDevArgs {
     int gate_stride;
     int T;
     int* err;
+    int group_m;  // m-tiles per rasterisation group (tile_coords)
 };
+
+// Tile t of the persistent walk -> (m-tile, n-tile).  Tiles go in groups of
+// group_m m-tiles; inside a group the walk is m-fastest across every n-tile.
+// A wave of CTAs then covers about group_m x (CTAs / group_m) tiles, so the A
+// panels it reads are shared by ~CTAs/group_m CTAs and the W panels by
+// group_m: operands that do not fit in L2 are read from DRAM a few times
+// instead of once per n-tile column.
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m, int& m, int& n) {
+    const int per_group = group_m * num_n;
+    const int g = t / per_group;
+    const int first = g * group_m;
+    const int gm = min(group_m, num_m - first);
+    const int r = t - g * per_group;
+    m = first + r % gm;
+    n = r / gm;
+}
 
 // GELU, tanh form: 0.5 v (1 + tanh(u)), u = sqrt(2/pi) (v + 0.044715 v^3),
 // evaluated through the identity 0.5 (1 + tanh(u)) = 1 / (1 + 2^(-2 u log2 e))
@@ -193,8 +214,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         long issued = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const int m0 = (tile % num_m) * kGemmBM;
-            const int n0 = (tile / num_m) * BN;
+            int mt, nt;
+            tile_coords(tile, num_m, num_n, p.group_m, mt, nt);
+            const int m0 = mt * kGemmBM;
+            const int n0 = nt * BN;
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!__all_sync(kFullMask, mbar_wait_bounded(&empty[stage], phase ^ 1u, p.err, KERR_GEMM_PRODUCER))) {
                     ok = false;
@@ -268,8 +291,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const int m0 = (tile % num_m) * kGemmBM;
-            const int n0 = (tile / num_m) * BN;
+            int mt, nt;
+            tile_coords(tile, num_m, num_n, p.group_m, mt, nt);
+            const int m0 = mt * kGemmBM;
+            const int n0 = nt * BN;
             // uniform across the warp: the tcgen05.ld below is warp-collective
             if (!__all_sync(kFullMask, mbar_wait_bounded(&acc_full[acc], acc_phase, p.err, KERR_GEMM_EPILOGUE)))
                 break;
@@ -347,6 +372,21 @@ int gemm_block_n(int M, int N, int num_sms) {
     return best;
 }
 
+// m-tiles per rasterisation group.  While A (M x K bf16) fits comfortably in
+// the 129 MB L2, one group of all m-tiles (plain m-fastest order) is best:
+// every wave shares one W panel and A is read from DRAM once.  Past that, A
+// would be re-read from DRAM once per n-tile column, so the tiles go in
+// groups: a wave of `ctas` tiles covering g m-tiles and ctas/g n-tiles
+// reads g A panels (128 rows) and ctas/g W panels (BN rows), and
+// g = sqrt(ctas * BN / 128) minimises those bytes.  Measured on GB300: Video
+// and Large projections 17-32 % faster grouped, Deep qkv/fc1 3-5 % slower.
+static int gemm_group_m(int num_m, int BN, int ctas, int64_t a_bytes) {
+    constexpr int64_t kAFitsInL2 = 64ll << 20;
+    if (a_bytes <= kAFitsInL2) return num_m;
+    int g = (int)std::lround(std::sqrt((double)ctas * BN / kGemmBM));
+    return std::max(1, std::min(g, num_m));
+}
+
 template <int BN, int EPI>
 static int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmW, const CUtensorMap& tmOut,
                          const GemmDevArgs& d, cudaStream_t st, int num_sms) {
@@ -360,10 +400,13 @@ static int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmW, const C
                                           Cfg::kSmemBytes));
         configured[dev] = true;
     }
-    const int tiles = ((d.M + kGemmBM - 1) / kGemmBM) * ((d.N + BN - 1) / BN);
+    const int num_m = (d.M + kGemmBM - 1) / kGemmBM;
+    const int tiles = num_m * ((d.N + BN - 1) / BN);
     const int grid = tiles < num_sms ? tiles : num_sms;
+    GemmDevArgs dg = d;
+    dg.group_m = gemm_group_m(num_m, BN, grid, (int64_t)d.M * d.K * 2);
     DLO_CUDA_TRY(launch_pdl(gemm_bf16_tcgen05<BN, EPI>, dim3(grid), dim3(kGemmThreads), Cfg::kSmemBytes, st, tmA, tmW,
-                            tmOut, d));
+                            tmOut, dg));
     DLO_CUDA_TRY(cudaGetLastError());
     return DLO_OK;
 }
@@ -374,7 +417,7 @@ int launch_gemm(const CUtensorMap& tmA, const CUtensorMap* tmWs, const GemmArgs&
     if (!a.bias || !a.out || !a.err) return set_error(DLO_ERR_INVALID_ARG, "gemm: null pointer");
     if (a.epilogue == DLO_EPI_GATED_RESIDUAL && (!a.gate || a.T <= 0 || a.gate_stride % 4))
         return set_error(DLO_ERR_INVALID_ARG, "gemm: gated residual needs gate, T > 0, gate_stride % 4 == 0");
-    GemmDevArgs d{a.M, a.N, a.K, a.bias, a.gate, a.gate_stride, a.T, a.err};
+    GemmDevArgs d{a.M, a.N, a.K, a.bias, a.gate, a.gate_stride, a.T, a.err, 1};
     CUtensorMap out_local;
     const CUtensorMap* tmOut = a.out_map;
     if (!tmOut) {
