@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-profile", action="store_true", help="no per-kernel events in the timed region")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--clock-interval-ms", type=int, default=200, help="nvidia-smi sampling period; 0 = no sampling")
+    ap.add_argument("--contiguous-shards", action="store_true",
+                    help="allocate each block's dp shards back to back in one pinned buffer (one copy per fill)")
     ap.add_argument("--requests", type=int, default=0,
                     help="requests sharing each streamed block (default: the workload's own R); the fill per "
                          "block is fixed, so this sweeps how it is amortised")
@@ -264,7 +266,8 @@ def main():
     R, T, L, dp = cfg.requests, cfg.tokens, cfg.blocks, cfg.dp_size
     spec = (cfg.hidden, cfg.heads, cfg.mlp, cfg.cond_dim)
     specs = [spec] * L
-    ps = PinnedShards(specs, dp, lambda b, i, shape: synthetic.weight_bits(cfg.seed, b, i, shape))
+    ps = PinnedShards(specs, dp, lambda b, i, shape: synthetic.weight_bits(cfg.seed, b, i, shape),
+                      contiguous=args.contiguous_shards)
     fill = {"auto": dlo.DLO_FILL_AUTO, "memcpy": dlo.DLO_FILL_MEMCPY, "zerocopy": dlo.DLO_FILL_ZEROCOPY}[args.fill]
     profile = not args.no_profile
     # Steady state of a denoising loop: every forward prefetches the next
@@ -397,7 +400,8 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": cfg.describe(), "global_batch": R * world, "seq_len": T,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
-                   "l2": "flushed between steps (256 MB write)", "fill": args.fill},
+                   "l2": "flushed between steps (256 MB write)", "fill": args.fill,
+                   "shards": "contiguous" if args.contiguous_shards else "separate"},
         "block_forwards_per_s": L * world / (ms_step * 1e-3),
         "steady_state": "each forward prefetches the next call's block 0 (DLO_PREFETCH_NEXT)",
         "cold_ms_per_step": sum(cold_ms) / max(len(cold_ms), 1),
