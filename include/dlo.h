@@ -266,8 +266,10 @@ enum {
     DLO_EPI_GATED_RESIDUAL = 2 /* out fp32 [M,N] += gate[(row/T)*gate_stride + col] * (A.W^T + bias) */
 };
 /* A bf16 [M, K] (device, 16-byte aligned), W bf16 [N, K] (16-byte aligned),
- * bias bf16 [N]; N and K multiples of 8.  tcgen05 tensor cores, fp32
- * accumulation; T is only used by DLO_EPI_GATED_RESIDUAL. */
+ * bias bf16 [N], out and gate 16-byte aligned; N and K multiples of 8.
+ * tcgen05 tensor cores, fp32 accumulation; T is only used by
+ * DLO_EPI_GATED_RESIDUAL, whose increment is added into out at L2 (one add
+ * per element, so the result does not depend on scheduling). */
 int dlo_op_linear(int32_t epilogue, const uint16_t* A, const uint16_t* W, const uint16_t* bias,
                   int32_t M, int32_t N, int32_t K, void* out, const float* gate, int32_t gate_stride,
                   int32_t T, dlo_stream_t stream);
