@@ -78,10 +78,11 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi SM clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi SM and memory clocks, memory temperature and throttle reasons
+    sampled during the timed region."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_power_cap,clocks.mem,temperature.memory")
 
     def __init__(self, index: int, interval_ms: int = 200):
         self.index = index
@@ -113,22 +114,32 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
+        sm, mx, mem, tmem, reasons = [], [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:  # "[N/A]" and the like
+                return None
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
-            if len(f) < 8:
+            if len(f) < 8 or num(f[0]) is None or num(f[1]) is None:
                 continue
-            try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
-            except ValueError:
-                continue
+            sm.append(num(f[0]))
+            mx.append(num(f[1]))
             for n, v in zip(names, f[4:8]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            if len(f) >= 10:
+                if num(f[8]) is not None:
+                    mem.append(num(f[8]))
+                if num(f[9]) is not None:
+                    tmem.append(num(f[9]))
+        med = lambda v: float(np.median(v)) if v else None
+        return {"sm_mhz": med(sm), "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm), "mem_mhz": med(mem), "mem_mhz_min": min(mem) if mem else None,
+                "mem_temp_c_max": max(tmem) if tmem else None}
 
 
 def max_over_ranks(x: float, dist=None, device: str = "cuda") -> float:
