@@ -426,7 +426,8 @@ def main():
         "e2e": {"value": job_throughput(tokens, world, e2e_step), "unit": "tokens/s",
                 "h2d_bytes_per_step": xh.numel() * 4 + ch.numel() * 4, "d2h_bytes_per_step": xh.numel() * 4},
         "gpu_launches": launches,
-        "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "mem_mhz", "mem_mhz_min",
+                                          "mem_temp_c_max")},
         "weights": {"fill_mode": {1: "memcpy", 2: "zerocopy"}.get(st["fill_mode"]),
                     "h2d_memcpy_gbs": st["h2d_memcpy_gbs"], "h2d_zerocopy_gbs": st["h2d_zerocopy_gbs"],
                     "device_weight_bytes": st["device_weight_high_water"], "slot_bytes": st["slot_bytes"],
