@@ -174,6 +174,35 @@ def test_linear_rows_independent_of_batch():
     assert torch.equal(big[300:400], small)
 
 
+def test_linear_grouped_tile_order_vs_oracle():
+    """An A operand above 64 MB switches the GEMM to grouped tile order (ragged
+    M, N and K, so the last group and the edge tiles are partial).  Sampled
+    rows match the oracle, and match bit for bit the same rows computed by a
+    small launch, which walks its tiles in plain order."""
+    M, N, K = 8229, 1000, 4200  # A = 69 MB
+    T = 2743
+    R = (M + T - 1) // T
+    A, Ab = bf16_tensor(9, 1, (M, K), 1.0)
+    W, Wb = bf16_tensor(9, 2, (N, K), 0.05)
+    bias, bb = bf16_tensor(9, 3, (N,), 0.1)
+    gate, gn = f32_tensor(9, 4, (R, N), 0.3)
+    x, xn = f32_tensor(9, 5, (M, N))
+    dlo.dlo_op_linear(dlo.DLO_EPI_GATED_RESIDUAL, A, W, bias, M, N, K, x, gate, N, T)
+    dlo.dlo_op_check()
+    got = x.cpu().numpy()
+    rows = np.unique(np.concatenate([np.arange(0, M, 517), np.arange(M - 40, M), [127, 128, 2175, 2176]]))
+    Af = bf16_bits_to_f64(Ab).reshape(M, K)[rows]
+    lin = dit.linear(Af, bf16_bits_to_f64(Wb).reshape(N, K), bf16_bits_to_f64(bb))
+    ref = xn[rows] + gn[rows // T] * lin
+    np.testing.assert_allclose(got[rows], ref, rtol=0, atol=2e-5 * np.abs(ref).max())
+    # the last 129 rows again, alone (plain order), from the same starting x
+    sub = torch.from_numpy(xn[M - 129:].copy()).cuda()
+    dlo.dlo_op_linear(dlo.DLO_EPI_GATED_RESIDUAL, A[M - 129:].contiguous(), W, bias, 129, N, K, sub,
+                      gate[(M - 129) // T:].contiguous(), N, 129 if (M - 129) // T == (M - 1) // T else T)
+    dlo.dlo_op_check()
+    assert np.array_equal(sub.cpu().numpy().view(np.uint32), got[M - 129:].view(np.uint32))
+
+
 # ---------------------------------------------------------------- attention
 
 @pytest.mark.parametrize("R,T,H,d", [(1, 64, 1, 64), (2, 100, 3, 64), (1, 257, 2, 128), (1, 1024, 4, 128),
