@@ -41,6 +41,8 @@
 // across the warp (__any_sync / __all_sync).  Every wait is bounded; on
 // expiry the CTA records a code, drains its own copies and MMAs, frees TMEM
 // and returns.
+#include <atomic>
+
 #include "dlo_device.cuh"
 #include "dlo_internal.h"
 
@@ -418,11 +420,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
 template <int D>
 static int launch_attention_t(const uint16_t* qkv, int R, int T, int H, uint16_t* o, int* err, cudaStream_t st) {
     using Cfg = AttCfg<D>;
-    static bool configured[64] = {};
+    // per device, once: repeating cudaFuncSetAttribute from racing threads is harmless
+    static std::atomic<bool> configured[64];
     int dev = 0;
     DLO_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return set_error(DLO_ERR_INVALID_ARG, "device index %d out of range", dev);
-    if (!configured[dev]) {
+    if (!configured[dev].load(std::memory_order_acquire)) {
         DLO_CUDA_TRY(cudaFuncSetAttribute(attention_fwd_tcgen05<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           Cfg::kSmemAlloc));
         // the setmaxnreg split assumes the launch register count; refuse to
@@ -432,7 +435,7 @@ static int launch_attention_t(const uint16_t* qkv, int R, int T, int H, uint16_t
         if (fa.numRegs < kRegsAtLaunch)
             return set_error(DLO_ERR_UNSUPPORTED, "attention: kernel built with %d registers per thread, needs %d",
                              fa.numRegs, kRegsAtLaunch);
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     CUtensorMap tm;
     const uint64_t h = (uint64_t)H * D;

@@ -28,6 +28,7 @@
 // Every wait is bounded (dlo_device.cuh); on expiry the kernel records an
 // error code, waits for its own copies and MMAs, frees TMEM and returns.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 
 #include "dlo_device.cuh"
@@ -391,14 +392,15 @@ template <int BN, int EPI>
 static int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmW, const CUtensorMap& tmOut,
                          const GemmDevArgs& d, cudaStream_t st, int num_sms) {
     using Cfg = GemmCfg<BN, EPI>;
-    static bool configured[64] = {};
+    // per device, once: repeating cudaFuncSetAttribute from racing threads is harmless
+    static std::atomic<bool> configured[64];
     int dev = 0;
     DLO_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return set_error(DLO_ERR_INVALID_ARG, "device index %d out of range", dev);
-    if (!configured[dev]) {
+    if (!configured[dev].load(std::memory_order_acquire)) {
         DLO_CUDA_TRY(cudaFuncSetAttribute(gemm_bf16_tcgen05<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           Cfg::kSmemBytes));
-        configured[dev] = true;
+        configured[dev].store(true, std::memory_order_release);
     }
     const int num_m = (d.M + kGemmBM - 1) / kGemmBM;
     const int tiles = num_m * ((d.N + BN - 1) / BN);
