@@ -219,24 +219,26 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             constexpr uint32_t idesc_s = umma_idesc_bf16_f32(kAttBM, kAttBN);
             constexpr uint32_t idesc_pv = umma_idesc_bf16_f32(kAttBM, D) | (1u << 16);  // B (= V) MN-major
             // S(t, j) = Q_t K_j^T into tile t's S columns
+            // Descriptors are built once per call and advanced by adding the
+            // byte offset / 16 to their start-address field (addresses stay
+            // below 256 KB, so the 14-bit field never carries).
             auto issue_s = [&](int t, int j) {
-                const uint32_t q_addr = smem_u32(sQ + t * Cfg::kQBytes);
-                const uint32_t k_addr = smem_u32(sK + (j % ST) * Cfg::kKVBytes);
+                const uint64_t qd = umma_desc_sw128(smem_u32(sQ + t * Cfg::kQBytes));
+                const uint64_t kd = umma_desc_sw128(smem_u32(sK + (j % ST) * Cfg::kKVBytes));
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)((kk >> 2) * kTileBytes + (kk & 3) * 32);
-                    umma_bf16(tmem + Cfg::s_col(t), umma_desc_sw128(q_addr + off), umma_desc_sw128(k_addr + off),
-                              idesc_s, kk > 0);
+                    const uint64_t off = (uint64_t)(((kk >> 2) * kTileBytes + (kk & 3) * 32) >> 4);
+                    umma_bf16(tmem + Cfg::s_col(t), qd + off, kd + off, idesc_s, kk > 0);
                 }
                 umma_commit(&s_full[t]);
             };
             // O_t += P(t, j) V_j, P from TMEM (16 keys = 8 packed columns per step)
             auto issue_pv = [&](int t, int j) {
-                const uint32_t v_addr = smem_u32(sV + (j % ST) * Cfg::kKVBytes);
+                const uint64_t vd = umma_desc_sw128_mn(smem_u32(sV + (j % ST) * Cfg::kKVBytes), kTileBytes);
+                const uint32_t pt = tmem + Cfg::p_col(t), ot = tmem + Cfg::o_col(t);
 #pragma unroll
                 for (int kk = 0; kk < kAttBN / 16; ++kk)
-                    umma_bf16_ts(tmem + Cfg::o_col(t), tmem + Cfg::p_col(t) + (uint32_t)(kk * 8),
-                                 umma_desc_sw128_mn(v_addr + (uint32_t)(kk * 2048), kTileBytes), idesc_pv,
+                    umma_bf16_ts(ot, pt + (uint32_t)(kk * 8), vd + (uint64_t)(kk * (2048 >> 4)), idesc_pv,
                                  (j > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(&o_done[t]);
             };

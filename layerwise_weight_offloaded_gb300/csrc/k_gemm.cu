@@ -263,13 +263,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     break;
                 }
                 tc_fence_after();
+                // descriptors advance by (32 bytes per K step) / 16 in their start-address field
                 const uint32_t a_addr = smem_u32(smem + stage * Cfg::kStageBytes);
-                const uint32_t b_addr = a_addr + Cfg::kABytes;
+                const uint64_t ad = umma_desc_sw128(a_addr), bd = umma_desc_sw128(a_addr + Cfg::kABytes);
 #pragma unroll
-                for (int k = 0; k < kGemmBK / 16; ++k) {
-                    umma_bf16(d_tmem, umma_desc_sw128(a_addr + k * 32), umma_desc_sw128(b_addr + k * 32), idesc,
-                              (kb | k) != 0);
-                }
+                for (int k = 0; k < kGemmBK / 16; ++k)
+                    umma_bf16(d_tmem, ad + (uint64_t)(k * 2), bd + (uint64_t)(k * 2), idesc, (kb | k) != 0);
                 umma_commit(&empty[stage]);  // stage is free once these MMAs have read it
                 if (++stage == S) {
                     stage = 0;
