@@ -43,7 +43,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-profile", action="store_true", help="no per-kernel events in the timed region")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--clock-interval-ms", type=int, default=200, help="nvidia-smi sampling period; 0 = no sampling")
+    ap.add_argument("--clock-interval-ms", type=int, default=50, help="nvidia-smi sampling period; 0 = no sampling")
     ap.add_argument("--contiguous-shards", action="store_true",
                     help="allocate each block's dp shards back to back in one pinned buffer (one copy per fill)")
     ap.add_argument("--requests", type=int, default=0,
