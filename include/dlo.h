@@ -241,6 +241,14 @@ int dlo_get_kernel_times(dlo_handle* h, double* ms, int64_t* launches);
  * bytes of the slot to host memory dst (bytes <= slot_bytes). */
 int dlo_debug_fill_and_read(dlo_handle* h, int32_t block, int32_t slot, void* dst, int64_t bytes);
 
+/* Test access to the failure path of a slot fill: the n-th fill issued from
+ * now on (n >= 1; 0 disarms) fails on the host before anything is enqueued,
+ * with DLO_ERR_CUDA ("injected fill failure") - a stand-in for a copy call
+ * that reports an error.  The call that meets it fails the handle closed, as
+ * a real copy error would: later calls return DLO_ERR_STATE and
+ * dlo_destroy still releases everything. */
+int dlo_debug_fail_fill(dlo_handle* h, int32_t n);
+
 /* Releases everything the handle owns (waits for its work first). */
 int dlo_destroy(dlo_handle* h);
 

@@ -44,7 +44,7 @@ EXPORTED = (
     "dlo_last_error", "dlo_status_string", "dlo_create", "dlo_forward", "dlo_forward_host", "dlo_synchronize",
     "dlo_get_stats", "dlo_get_kernel_times", "dlo_debug_fill_and_read", "dlo_destroy", "dlo_op_adaln",
     "dlo_op_ln_modulate", "dlo_op_linear", "dlo_op_attention", "dlo_op_shard_gather", "dlo_op_check",
-    "dlo_op_linear_noalloc", "dlo_forward_steps",
+    "dlo_op_linear_noalloc", "dlo_forward_steps", "dlo_debug_fail_fill",
 )
 
 
@@ -91,6 +91,7 @@ _SIGS = {
     "dlo_get_stats": [_c_p, ctypes.POINTER(dlo_stats)],
     "dlo_get_kernel_times": [_c_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_c_i64)],
     "dlo_debug_fill_and_read": [_c_p, _c_i32, _c_i32, _c_p, _c_i64],
+    "dlo_debug_fail_fill": [_c_p, _c_i32],
     "dlo_destroy": [_c_p],
     "dlo_op_adaln": [_c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_p, _c_p],
     "dlo_op_ln_modulate": [_c_p, _c_p, _c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p],
@@ -251,6 +252,11 @@ def dlo_get_kernel_times(handle: int) -> dict:
 
 def dlo_debug_fill_and_read(handle: int, block: int, slot: int, dst, nbytes: int) -> None:
     _check(lib().dlo_debug_fill_and_read(handle, block, slot, _ptr(dst), nbytes))
+
+
+def dlo_debug_fail_fill(handle: int, n: int) -> None:
+    """Makes the n-th slot fill from now on fail on the host (0 disarms)."""
+    _check(lib().dlo_debug_fail_fill(handle, n))
 
 
 def dlo_destroy(handle: int) -> None:

@@ -200,6 +200,7 @@ struct dlo_handle {
     int64_t act_rows = -1;  // rows the activation maps were encoded for
     std::vector<ActMaps> amaps;
     const float* x_map_ptr = nullptr;  // x the amaps' x_out maps were encoded for (rows = act_rows)
+    int fail_fill_in = 0;  // dlo_debug_fail_fill: fills until the injected failure (0 = none)
     // host-buffer forward staging
     float* x_dev = nullptr;
     float* c_dev = nullptr;
@@ -227,6 +228,7 @@ void add_weight_bytes(dlo_handle* h, int64_t b) {
 
 // Issues the rebuild of block b into `dst` on the copy stream.
 int issue_fill(dlo_handle* h, int b, uint16_t* dst, int mode) {
+    if (h->fail_fill_in > 0 && --h->fail_fill_in == 0) return set_error(DLO_ERR_CUDA, "injected fill failure");
     const int64_t S = h->S[b];
     const int64_t bytes = S * 2;
     if (mode == DLO_FILL_ZEROCOPY) {
@@ -760,6 +762,13 @@ int dlo_get_kernel_times(dlo_handle* h, double* ms, int64_t* launches) {
         ms[e.cls] += t;
         launches[e.cls] += 1;
     }
+    return DLO_OK;
+}
+
+int dlo_debug_fail_fill(dlo_handle* h, int32_t n) {
+    if (!h) return set_error(DLO_ERR_INVALID_ARG, "debug_fail_fill: null handle");
+    if (n < 0) return set_error(DLO_ERR_INVALID_ARG, "debug_fail_fill: n must be >= 0");
+    h->fail_fill_in = n;
     return DLO_OK;
 }
 

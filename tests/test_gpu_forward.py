@@ -320,6 +320,81 @@ def test_host_side_timeout_and_error_state():
         run.close()
 
 
+@pytest.mark.parametrize("flags", [dlo.DLO_FILL_MEMCPY, dlo.DLO_FILL_ZEROCOPY | dlo.DLO_PREFETCH_NEXT])
+def test_injected_fill_failure_fails_the_handle_closed(flags):
+    """A slot fill whose copy call reports an error (injected on the host, no
+    GPU fault) fails that forward with DLO_ERR_CUDA; the handle stays closed
+    (DLO_ERR_STATE) and is still destroyed cleanly.  A fresh handle over the
+    same shards is unaffected."""
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * 4
+    x, c = inputs((1, 64, cfg.hidden, cfg.cond_dim), 50)
+    good = Run(specs, 2, 4, flags)
+    try:
+        want = good.forward(x, c)
+    finally:
+        good.close()
+    run = Run(specs, 2, 4, flags)
+    try:
+        ok = run.forward(x, c)  # a healthy first forward
+        assert np.array_equal(ok.view(np.uint32), want.view(np.uint32))
+        dlo.dlo_debug_fail_fill(run.h, 3)
+        xd, cd = torch.from_numpy(x).cuda(), torch.from_numpy(c).cuda()
+        with pytest.raises(dlo.DloError) as e:
+            dlo.dlo_forward(run.h, xd, cd, 1, 64, torch.cuda.current_stream())
+        assert e.value.status == dlo.DLO_ERR_CUDA and "injected" in str(e.value)
+        with pytest.raises(dlo.DloError) as e:
+            dlo.dlo_forward(run.h, xd, cd, 1, 64, torch.cuda.current_stream())
+        assert e.value.status == dlo.DLO_ERR_STATE
+        torch.cuda.synchronize()
+    finally:
+        run.close()  # releases the handle after the partial forward
+    again = Run(specs, 2, 4, flags)
+    try:
+        assert np.array_equal(again.forward(x, c).view(np.uint32), want.view(np.uint32))
+    finally:
+        again.close()
+
+
+def test_pageable_shards():
+    """Shards in ordinary (pageable) host memory.  The zero-copy fill needs
+    shards the device can address: create refuses it with DLO_ERR_INVALID_ARG
+    unless the platform reports the memory as device-accessible (address
+    translation services), in which case it must stream correctly.  The
+    copy-engine fill streams them and gives the pinned result bit for bit."""
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * 3
+    src = param_source(7)
+    n = dlo.dlo_block_numel(specs[0])
+    S = dlo.dlo_shard_numel(n, 2)
+    shards = [[np.zeros(S, np.uint16) for _ in range(2)] for _ in specs]
+    for b, sp in enumerate(specs):
+        params = [np.ascontiguousarray(src(b, i, shape)).reshape(-1) for i, shape in enumerate(pinned_param_shapes(sp))]
+        dlo.dlo_pack_block(sp, params, 2, shards[b])
+    ptrs = [a.ctypes.data for blk in shards for a in blk]
+    x, c = inputs((2, 50, cfg.hidden, cfg.cond_dim), 51)
+    pinned = Run(specs, 2, 7, dlo.DLO_FILL_MEMCPY)
+    try:
+        want = pinned.forward(x, c)
+    finally:
+        pinned.close()
+    modes = [dlo.DLO_FILL_MEMCPY, dlo.DLO_FILL_AUTO]
+    try:
+        dlo.dlo_destroy(dlo.dlo_create(specs, 2, ptrs, dlo.DLO_FILL_ZEROCOPY))
+        modes.append(dlo.DLO_FILL_ZEROCOPY)  # reported device-accessible: it must stream correctly too
+    except dlo.DloError as e:
+        assert e.status == dlo.DLO_ERR_INVALID_ARG
+    for flags in modes:
+        h = dlo.dlo_create(specs, 2, ptrs, flags)
+        try:
+            xd, cd = torch.from_numpy(x).cuda(), torch.from_numpy(c).cuda()
+            dlo.dlo_forward(h, xd, cd, 2, 50, torch.cuda.current_stream())
+            dlo.dlo_synchronize(h, 60000)
+            assert np.array_equal(xd.cpu().numpy().view(np.uint32), want.view(np.uint32))
+        finally:
+            dlo.dlo_destroy(h)
+
+
 def test_invalid_forward_arguments():
     cfg = synthetic.get_config("tiny")
     run = Run([spec_tuple(cfg)], 2)
