@@ -317,12 +317,12 @@ int ensure_activations(dlo_handle* h, int R, int T) {
         h->st.activation_bytes = 0;
         (void)dummy;
         const int64_t hd = h->hidden;
-        DLO_CUDA_TRY(cudaMalloc(&h->mod, (size_t)reqs * 6 * hd * sizeof(float)));
+        DLO_CUDA_TRY(cudaMalloc(&h->mod, (size_t)2 * reqs * 6 * hd * sizeof(float)));  // one per block parity
         DLO_CUDA_TRY(cudaMalloc(&h->u, (size_t)rows * hd * 2));
         DLO_CUDA_TRY(cudaMalloc(&h->qkv, (size_t)rows * 3 * hd * 2));
         DLO_CUDA_TRY(cudaMalloc(&h->o, (size_t)rows * hd * 2));
         DLO_CUDA_TRY(cudaMalloc(&h->g, (size_t)rows * h->max_mlp * 2));
-        h->st.activation_bytes = reqs * 6 * hd * 4 + rows * hd * 2 * 5 + rows * (int64_t)h->max_mlp * 2;
+        h->st.activation_bytes = 2 * reqs * 6 * hd * 4 + rows * hd * 2 * 5 + rows * (int64_t)h->max_mlp * 2;
         h->rows_cap = rows;
         h->req_cap = reqs;
         h->act_rows = -1;
@@ -354,24 +354,42 @@ int ensure_x_maps(dlo_handle* h, float* x, int64_t M) {
     return DLO_OK;
 }
 
-// The kernels of one block, weights read from `slot`, all on the compute stream `s`.
-int run_block(dlo_handle* h, int b, int slot, float* x, const float* cond, int R, int T, cudaStream_t s) {
+// Block b's modulation vectors: one buffer per block parity, so the adaLN of
+// block b+1 can run while block b still reads its own.
+float* mod_buf(dlo_handle* h, int b) { return h->mod + (size_t)(b & 1) * h->req_cap * 6 * h->hidden; }
+
+// The adaLN GEMV of block b (its weights in `slot`) on stream `st`.
+int run_adaln(dlo_handle* h, int b, int slot, const float* cond, int R, cudaStream_t st) {
+    const auto& sp = h->specs[b];
+    const uint16_t* w = weights_base(h, b, h->resident ? 0 : slot);
+    ProfEvent* e = prof_begin(h, DLO_K_ADALN, st);
+    int rc = launch_adaln(w + h->off[b][DLO_P_ADA_W], w + h->off[b][DLO_P_ADA_B], cond, R, sp.cond_dim,
+                          6 * sp.hidden, mod_buf(h, b), st);
+    if (rc) return rc;
+    prof_end(e, st);
+    h->st.kernel_launches++;
+    return DLO_OK;
+}
+
+// The kernels of one block, weights read from `slot`, all on the compute stream
+// `s`; its adaLN too unless `adaln_done` (then it ran on the copy stream right
+// after the block's fill, off the compute stream's critical path).
+int run_block(dlo_handle* h, int b, int slot, float* x, const float* cond, int R, int T, cudaStream_t s,
+              bool adaln_done) {
     const auto& sp = h->specs[b];
     const auto& of = h->off[b];
-    const int hd = sp.hidden, H = sp.num_heads, d = hd / H, m = sp.mlp_hidden, C = sp.cond_dim;
+    const int hd = sp.hidden, H = sp.num_heads, d = hd / H, m = sp.mlp_hidden;
     const int M = R * T;
     if (h->resident) slot = 0;
     const uint16_t* w = weights_base(h, b, slot);
     const BlockMaps& bm = h->maps[b][slot];
     const ActMaps& am = h->amaps[b];
-    float* mod = h->mod;
+    float* mod = mod_buf(h, b);
     const int ms = 6 * hd;
     int rc;
     ProfEvent* e;
 
-    e = prof_begin(h, DLO_K_ADALN, s);
-    if ((rc = launch_adaln(w + of[DLO_P_ADA_W], w + of[DLO_P_ADA_B], cond, R, C, 6 * hd, mod, s))) return rc;
-    prof_end(e, s);
+    if (!adaln_done && (rc = run_adaln(h, b, slot, cond, R, s))) return rc;
 
     e = prof_begin(h, DLO_K_LN_MOD, s);
     if ((rc = launch_ln_modulate(x, mod + 0 * hd, mod + 1 * hd, ms, R, T, hd, h->u, s))) return rc;
@@ -414,7 +432,7 @@ int run_block(dlo_handle* h, int b, int slot, float* x, const float* cond, int R
     if ((rc = launch_gemm(am.g, bm.fc2, a, s, h->dev.num_sms))) return rc;
     prof_end(e, s);
 
-    h->st.kernel_launches += 8;
+    h->st.kernel_launches += 7;
     return DLO_OK;
 }
 
@@ -621,17 +639,21 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
     const int base = (!h->resident && h->prefetch) ? h->next_base : 0;
     auto slot_of = [&](int N) { return (base + N) & 1; };
     if (!h->resident) {
-        if (prefetched) {
-            // The activation scratch is shared: run after the previous forward
-            // (which may have been issued on another stream).
-            FWD_TRY(cudaStreamWaitEvent(s, h->done_ev, 0));
-        } else {
-            // Slots may still be read by earlier work on `s`: the first fill waits for it.
-            FWD_TRY(cudaEventRecord(h->start_ev, s));
-            FWD_TRY(cudaStreamWaitEvent(h->copy, h->start_ev, 0));
+        // The copy stream joins the caller's order at the start of every call:
+        // the slots may still be read by earlier work on `s`, and the adaLN
+        // GEMVs it runs after each fill read this call's cond.
+        FWD_TRY(cudaEventRecord(h->start_ev, s));
+        FWD_TRY(cudaStreamWaitEvent(h->copy, h->start_ev, 0));
+        // The slots, the modulation buffers and the activation scratch are
+        // shared with the previous forward, which may have been issued on
+        // another stream (an event never recorded counts as complete).
+        FWD_TRY(cudaStreamWaitEvent(h->copy, h->done_ev, 0));
+        FWD_TRY(cudaStreamWaitEvent(s, h->done_ev, 0));
+        if (!prefetched) {
             ProfEvent* pe = prof_begin(h, DLO_K_FILL, h->copy);
             if ((rc = issue_fill(h, 0, h->slot[slot_of(0)], h->fill_mode))) return fail(h, rc);
             prof_end(pe, h->copy);
+            if ((rc = run_adaln(h, 0, slot_of(0), cond, R, h->copy))) return fail(h, rc);
             FWD_TRY(cudaEventRecord(h->filled[slot_of(0)], h->copy));
         }
     }
@@ -646,13 +668,17 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
                 ProfEvent* pe = prof_begin(h, DLO_K_FILL, h->copy);
                 if ((rc = issue_fill(h, N + 1, h->slot[ns], h->fill_mode))) return fail(h, rc);
                 prof_end(pe, h->copy);
+                // the next block's modulation, beside this block's compute
+                if ((rc = run_adaln(h, N + 1, ns, cond, R, h->copy))) return fail(h, rc);
                 FWD_TRY(cudaEventRecord(h->filled[ns], h->copy));
             }
             ProfEvent* pw = prof_begin(h, DLO_K_FILL_WAIT, s);
             FWD_TRY(cudaStreamWaitEvent(s, h->filled[slot], 0));
             prof_end(pw, s);
         }
-        if ((rc = run_block(h, N, slot, x, cond, R, T, s))) return fail(h, rc);
+        // a prefetched block 0 was filled by the previous call, whose cond may differ
+        const bool adaln_done = !h->resident && !(N == 0 && prefetched);
+        if ((rc = run_block(h, N, slot, x, cond, R, T, s, adaln_done))) return fail(h, rc);
         if (!h->resident) FWD_TRY(cudaEventRecord(h->freed[slot], s));
     }
     if (!h->resident && h->prefetch) {
