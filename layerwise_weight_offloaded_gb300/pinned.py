@@ -33,7 +33,10 @@ class PinnedShards:
     """
 
     def __init__(self, specs: Sequence, dp_size: int,
-                 param_source: Callable[[int, int, tuple], np.ndarray], contiguous: bool = False):
+                 param_source: Callable[[int, int, tuple], np.ndarray], contiguous: bool = False,
+                 pin: bool = True):
+        """pin=False allocates ordinary host memory instead (the copy-engine fill
+        still streams it; zero-copy needs device-addressable memory)."""
         import torch
 
         self.specs = [B._spec(s) for s in specs]
@@ -44,11 +47,11 @@ class PinnedShards:
             n = B.dlo_block_numel(sp)
             S = B.dlo_shard_numel(n, dp_size)
             if contiguous:
-                buf = torch.empty(S * dp_size, dtype=torch.int16, pin_memory=True)
+                buf = torch.empty(S * dp_size, dtype=torch.int16, pin_memory=pin)
                 self._keep.append(buf)
                 shards = [buf[r * S:(r + 1) * S] for r in range(dp_size)]
             else:
-                shards = [torch.empty(S, dtype=torch.int16, pin_memory=True) for _ in range(dp_size)]
+                shards = [torch.empty(S, dtype=torch.int16, pin_memory=pin) for _ in range(dp_size)]
             params = [np.ascontiguousarray(param_source(b, i, shape), dtype=np.uint16).reshape(-1)
                       for i, shape in enumerate(param_shapes(sp))]
             for p, shape in zip(params, param_shapes(sp)):
@@ -79,7 +82,8 @@ def block_flat_offsets(specs: Sequence) -> list[int]:
     return offs
 
 
-def pack_from_flat_file(path: str, specs: Sequence, dp_size: int, contiguous: bool = False) -> "PinnedShards":
+def pack_from_flat_file(path: str, specs: Sequence, dp_size: int, contiguous: bool = False,
+                        pin: bool = True) -> "PinnedShards":
     """Pinned shards packed straight from a memory-mapped flat bf16 weight file.
 
     Section 1 of "vLLM-Omni 发布 Distributed Layerwise Offload…" builds the
@@ -106,7 +110,7 @@ def pack_from_flat_file(path: str, specs: Sequence, dp_size: int, contiguous: bo
             start = offs[b] + p_off[i]
             return flat[start:start + p_num[i]]
 
-        ps = PinnedShards(specs, dp_size, source, contiguous=contiguous)
+        ps = PinnedShards(specs, dp_size, source, contiguous=contiguous, pin=pin)
     finally:
         mapped = flat.size * 2
         del flat  # unmaps the file

@@ -8,6 +8,7 @@ import pytest
 
 import layerwise_weight_offloaded_gb300 as dlo
 from layerwise_weight_offloaded_gb300 import build as dlo_build
+import synthetic
 from oracle import dit, shards
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -134,3 +135,33 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(B, "_lib", None)
     with pytest.raises(B.DloLibraryMissing):
         B.dlo_block_numel((64, 1, 8, 8))
+
+
+def test_pack_from_mmapped_flat_file_vs_oracle(tmp_path):
+    """NEXT-3 on the host: shards packed straight from a memory-mapped flat
+    weight file (blocks back to back in parameter-table order) equal the
+    oracle's packing of each block's flat buffer, bit for bit, padding
+    included."""
+    from layerwise_weight_offloaded_gb300.pinned import block_flat_offsets, pack_from_flat_file
+
+    specs = [(128, 2, 256, 32), (64, 1, 96, 32), (256, 2, 128, 32)]
+    dp = 5
+    flats = []
+    for b, (h, H, m, C) in enumerate(specs):
+        parts = [synthetic.weight_bits(9, b, i, shape).reshape(-1)
+                 for i, (_, shape) in enumerate(dit.param_shapes(h, m, C))]
+        flats.append(np.concatenate(parts))
+    path = tmp_path / "blocks.bf16"
+    np.concatenate(flats).astype(np.uint16).tofile(path)
+    offs = block_flat_offsets(specs)
+    assert offs == [0, flats[0].size, flats[0].size + flats[1].size]
+    ps = pack_from_flat_file(str(path), specs, dp, pin=False)
+    assert ps.mapped_bytes == path.stat().st_size
+    for b in range(len(specs)):
+        want = shards.pack(flats[b], dp)
+        for r in range(dp):
+            assert np.array_equal(ps.shard_numpy(b, r), want[r]), (b, r)
+    short = tmp_path / "short.bf16"
+    np.zeros(10, np.uint16).tofile(short)
+    with pytest.raises(ValueError):
+        pack_from_flat_file(str(short), specs, dp, pin=False)
