@@ -6,7 +6,10 @@
 // O = softmax(Q K^T / sqrt(d)) V: fp32 logits in TMEM, fp32 online softmax,
 // softmax weights rounded to bf16 for the P.V product, fp32 accumulation.
 //
-// One CTA = two 128-row query tiles of one (request, head), 12 warps:
+// One CTA = two 128-row query tiles of one (request, head), 12 warps.  At
+// d = 128, when the last wave of such pairs would leave more than half the
+// SMs idle, those pairs run as one CTA per tile instead (the second softmax
+// warpgroup idles).
 //   warp 0     TMA producer: both Q tiles once, then 128-key K and V tiles into
 //              a STAGES-deep ring shared by the two query tiles (3-D tensor map
 //              over [R, T, 3h]: a tile never reaches into the next request,
@@ -117,7 +120,7 @@ enum : int {
 template <int D>
 __global__ void __launch_bounds__(kAttThreads, 1)
     attention_fwd_tcgen05(const __grid_constant__ CUtensorMap tm, int T, int H, uint16_t* __restrict__ o,
-                          float scale_log2, int* err) {
+                          float scale_log2, int n_pairs, int split_from, int* err) {
     using Cfg = AttCfg<D>;
     constexpr int ST = Cfg::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -139,9 +142,29 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int q0 = blockIdx.x * 2 * kAttBM;
-    const int head = blockIdx.y;
-    const int req = blockIdx.z;
+    // Work units are pairs of 128-row query tiles of one (request, head).  At
+    // d = 128 the grid is 1-D: CTAs below split_from take a whole pair, the
+    // units from split_from on (the last partial wave) are split into one CTA
+    // per tile, so that wave ends in about half the time.  At d = 64 the grid
+    // is (pair, head, request) and every CTA takes a pair: the extra control
+    // flow measurably slowed the issue-bound MMA warp there.
+    constexpr bool kSplitTail = D == 128;
+    int q0, head, req, ntiles = 2;
+    if constexpr (kSplitTail) {
+        const int bid = (int)blockIdx.x;
+        const bool whole = bid < split_from;
+        const int unit = whole ? bid : split_from + (bid - split_from) / 2;
+        const int pair = unit % n_pairs;
+        ntiles = whole ? 2 : 1;
+        head = (unit / n_pairs) % H;
+        req = unit / (n_pairs * H);
+        q0 = (pair * 2 + (whole ? 0 : (bid - split_from) & 1)) * kAttBM;
+    } else {
+        q0 = blockIdx.x * 2 * kAttBM;
+        head = blockIdx.y;
+        req = blockIdx.z;
+    }
+    if (kSplitTail && q0 >= T) return;  // a single tile past the end of the request: nothing to do
     const int h = H * D;
     const int n_kv = (T + kAttBN - 1) / kAttBN;
 
@@ -160,6 +183,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             mbar_init(&o_done[t], 1);
         }
         mbar_init(drain, 1);
+        if constexpr (kSplitTail) {
+            tmem_slot[1] = q0;
+            tmem_slot[2] = req;
+            tmem_slot[3] = head;
+        }
         fence_mbarrier_init();
         tma_prefetch_desc(&tm);
     }
@@ -179,8 +207,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             // ---------------- TMA producer (whole warp; one elected lane issues)
             long issued_k = 0, issued_v = 0;
             if (elect_one()) {
-                mbar_arrive_expect_tx(q_full, 2 * Cfg::kQBytes);
-                for (int t = 0; t < 2; ++t)
+                mbar_arrive_expect_tx(q_full, ntiles * Cfg::kQBytes);
+                for (int t = 0; t < ntiles; ++t)
                     for (int c = 0; c < Cfg::kChunks; ++c)
                         tma_load_3d(sQ + t * Cfg::kQBytes + c * kTileBytes, &tm, head * D + c * 64, q0 + t * kAttBM,
                                     req, q_full);
@@ -249,7 +277,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
             if (ok) {
                 tc_fence_after();
                 issue_s(0, 0);
-                issue_s(1, 0);
+                if (ntiles == 2) issue_s(1, 0);
                 umma_commit(&k_empty[0]);
             }
             for (int j = 0; j < n_kv && ok; ++j) {
@@ -263,6 +291,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     // then PV(t, j) once it has written P; the two tiles do not wait
                     // on each other
                     for (int t = 0; t < 2 && ok; ++t) {
+                        if (t >= ntiles) break;  // a split tail CTA has one tile
                         if (next) {
                             if (!(ok = wait(&s_free[t], ph))) break;
                             tc_fence_after();
@@ -278,12 +307,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                     // which reads P there, has completed.  Both PVs are queued first so
                     // the tensor core stays busy while this warp waits.
                     for (int t = 0; t < 2 && ok; ++t) {
+                        if (t >= ntiles) break;  // a split tail CTA has one tile
                         if (!(ok = wait(&p_full[t], ph))) break;
                         tc_fence_after();
                         issue_pv(t, j);
                     }
                     if (ok && next) {
                         for (int t = 0; t < 2 && ok; ++t) {
+                            if (t >= ntiles) break;  // a split tail CTA has one tile
                             if (!(ok = wait(&o_done[t], ph))) break;
                             tc_fence_after();
                             issue_s(t, j + 1);
@@ -307,6 +338,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const uint32_t s_addr = tmem + lane_base + Cfg::s_col(t);
         const uint32_t p_addr = tmem + lane_base + Cfg::p_col(t);
         const uint32_t o_addr = tmem + lane_base + Cfg::o_col(t);
+        // the second warpgroup of a single-tile CTA has no work
+        if (!kSplitTail || t == 0 || (int)blockIdx.x < split_from) {
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
@@ -389,8 +422,17 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
-            const int t_row = q0 + t * kAttBM + row;
-            uint16_t* orow = o + ((size_t)req * T + t_row) * h + head * D;
+            // at d = 128 the tile's coordinates come back from shared memory:
+            // kept in registers through the loop they pushed the softmax into spills
+            int cq0 = q0, creq = req, chead = head;
+            if constexpr (kSplitTail) {
+                const volatile int* coords = reinterpret_cast<const volatile int*>(tmem_slot + 1);
+                cq0 = coords[0];
+                creq = coords[1];
+                chead = coords[2];
+            }
+            const int t_row = cq0 + t * kAttBM + row;
+            uint16_t* orow = o + ((size_t)creq * T + t_row) * h + chead * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
@@ -409,6 +451,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 }
             }
         }
+        }  // has a tile
     }
 
     tc_fence_before();
@@ -417,6 +460,14 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::kTmemCols);
     }
+}
+
+// Number of pair units at the front that run as whole pairs (see the kernel):
+// when the last wave of pair units would be less than half full, those units
+// are split into single-tile CTAs instead.
+static int attention_split_from(long units, int num_sms) {
+    const long rem = units % num_sms;
+    return (rem > 0 && 2 * rem <= num_sms) ? (int)(units - rem) : (int)units;
 }
 
 template <int D>
@@ -444,9 +495,19 @@ static int launch_attention_t(const uint16_t* qkv, int R, int T, int H, uint16_t
     int rc = encode_tmap_bf16_3d(&tm, qkv, 3 * h, (uint64_t)T, (uint64_t)R, 128);
     if (rc) return rc;
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-    dim3 grid((T + 2 * kAttBM - 1) / (2 * kAttBM), H, R);
+    DeviceInfo di;
+    if ((rc = device_info(&di))) return rc;
+    const int n_pairs = (T + 2 * kAttBM - 1) / (2 * kAttBM);
+    const long units = (long)R * H * n_pairs;
+    if (2 * units > 0x7FFFFFFFL) return set_error(DLO_ERR_SHAPE, "attention: too many query tiles");
+    int split_from = (int)units;
+    dim3 grid(n_pairs, H, R);
+    if (D == 128) {
+        split_from = attention_split_from(units, di.num_sms);
+        grid = dim3((unsigned)(split_from + 2 * (units - split_from)));
+    }
     DLO_CUDA_TRY(launch_pdl(attention_fwd_tcgen05<D>, grid, dim3(kAttThreads), Cfg::kSmemAlloc, st, tm, T, H, o,
-                            scale_log2, err));
+                            scale_log2, n_pairs, split_from, err));
     DLO_CUDA_TRY(cudaGetLastError());
     return DLO_OK;
 }
