@@ -417,6 +417,13 @@ def main():
                    "shards": "contiguous" if args.contiguous_shards else "separate"},
         "block_forwards_per_s": L * world / (ms_step * 1e-3),
         "steady_state": "each forward prefetches the next call's block 0 (DLO_PREFETCH_NEXT)",
+        # the copy stream's fill time against the compute stream's waits for it,
+        # from the profiled pass: how much of the host-to-device copy hides
+        # under compute
+        "copy_overlap": ({"fill_ms_per_step": ktime["fill"] / args.steps,
+                          "exposed_wait_ms_per_step": ktime["fill_wait"] / args.steps,
+                          "hidden_fraction": 1.0 - ktime["fill_wait"] / ktime["fill"]}
+                         if profile and ktime.get("fill", 0) > 0 else None),
         "cold_ms_per_step": sum(cold_ms) / max(len(cold_ms), 1),
         "step_ms": {"min": min(step_ms), "median": float(np.median(step_ms)), "max": max(step_ms)},
         "path_roofline": {"frac": path_frac, "per_block_roofline_ms": roof_block_s * 1e3,

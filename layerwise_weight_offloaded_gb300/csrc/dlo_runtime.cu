@@ -22,6 +22,8 @@
 
 #include "dlo_internal.h"
 
+#include <nvtx3/nvToolsExt.h>  // header-only; no-ops unless a profiler is attached
+
 namespace dlo {
 
 int cuda_error(cudaError_t e, const char* what) {
@@ -678,7 +680,10 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
         }
         // a prefetched block 0 was filled by the previous call, whose cond may differ
         const bool adaln_done = !h->resident && !(N == 0 && prefetched);
-        if ((rc = run_block(h, N, slot, x, cond, R, T, s, adaln_done))) return fail(h, rc);
+        nvtxRangePushA("dlo block");
+        rc = run_block(h, N, slot, x, cond, R, T, s, adaln_done);
+        nvtxRangePop();
+        if (rc) return fail(h, rc);
         if (!h->resident) FWD_TRY(cudaEventRecord(h->freed[slot], s));
     }
     if (!h->resident && h->prefetch) {
