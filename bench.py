@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-profile", action="store_true", help="no per-kernel events in the timed region")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--timeline-out", default="",
+                    help="write the per-interval timeline of the last profiled forward (JSON) to this path")
     ap.add_argument("--clock-interval-ms", type=int, default=200, help="nvidia-smi sampling period; 0 = no sampling")
     ap.add_argument("--contiguous-shards", action="store_true",
                     help="allocate each block's dp shards back to back in one pinned buffer (one copy per fill)")
@@ -245,6 +247,23 @@ def run_reference(args, cfg, rank, world):
     print(json.dumps(out), flush=True)
 
 
+def timeline_summary(events):
+    """Busy time of each stream and the compute stream's exposed waits in one
+    profiled forward (intervals from dlo_get_timeline, ms from its start)."""
+    if not events:
+        return None
+    busy = {"compute": 0.0, "copy": 0.0}
+    wait = 0.0
+    for e in events:
+        d = e["end_ms"] - e["start_ms"]
+        if e["kernel"] == "fill_wait":
+            wait += d
+        else:
+            busy[e["stream"]] += d
+    return {"span_ms": max(e["end_ms"] for e in events), "compute_busy_ms": busy["compute"],
+            "copy_busy_ms": busy["copy"], "fill_wait_ms": wait}
+
+
 def main():
     args = parse()
     import synthetic
@@ -334,25 +353,33 @@ def main():
     dlo.dlo_destroy(hc)
 
     # (B) per-kernel device times: a second timed pass of K forwards on a handle
-    # that records CUDA events around every launch (same fill mechanism); the
-    # events themselves lengthen the step, so (A) alone gives the headline.
+    # that records CUDA events around every launch (same fill mechanism, same
+    # cross-call prefetch); the events themselves lengthen the step, so (A)
+    # alone gives the headline.
     kclasses = dlo.KERNEL_CLASSES
     ktime = {k: 0.0 for k in kclasses}
     klaunch = {k: 0 for k in kclasses}
     prof_step_ms = []
+    timeline = []
     if profile:
-        hp = dlo.dlo_create(specs, dp, ps.ptrs, dlo.dlo_get_stats(h)["fill_mode"] | dlo.DLO_PROFILE)
+        hp = dlo.dlo_create(specs, dp, ps.ptrs,
+                            dlo.dlo_get_stats(h)["fill_mode"] | dlo.DLO_PROFILE | dlo.DLO_PREFETCH_NEXT)
 
         def collect():
             for k, (ms, n) in dlo.dlo_get_kernel_times(hp).items():
                 ktime[k] += ms
                 klaunch[k] += n
+            timeline[:] = dlo.dlo_get_timeline(hp)
 
         x.copy_(x0)
         dlo.dlo_forward(hp, x, cond, R, T, stream)  # warm-up of the profiled handle
         dlo.dlo_synchronize(hp, 600000)
         prof_step_ms = timed_steps(hp, args.steps, collect)
         dlo.dlo_destroy(hp)
+        if args.timeline_out and rank == 0:
+            with open(args.timeline_out, "w") as f:
+                json.dump({"workload": args.workload, "blocks": L, "fill_mode": dlo.dlo_get_stats(h)["fill_mode"],
+                           "events": timeline}, f, indent=0)
 
     # the clock samples span the headline pass (A), the cold pass and the profiled pass (B)
     clk = clocks.stop()
@@ -422,7 +449,8 @@ def main():
         # under compute
         "copy_overlap": ({"fill_ms_per_step": ktime["fill"] / args.steps,
                           "exposed_wait_ms_per_step": ktime["fill_wait"] / args.steps,
-                          "hidden_fraction": 1.0 - ktime["fill_wait"] / ktime["fill"]}
+                          "hidden_fraction": 1.0 - ktime["fill_wait"] / ktime["fill"],
+                          "last_step": timeline_summary(timeline)}
                          if profile and ktime.get("fill", 0) > 0 else None),
         "cold_ms_per_step": sum(cold_ms) / max(len(cold_ms), 1),
         "step_ms": {"min": min(step_ms), "median": float(np.median(step_ms)), "max": max(step_ms)},

@@ -236,6 +236,25 @@ int dlo_get_stats(dlo_handle* h, dlo_stats* out);
  * Both arrays hold DLO_K_NUM entries. */
 int dlo_get_kernel_times(dlo_handle* h, double* ms, int64_t* launches);
 
+/* One profiled interval of a forward: a kernel, a slot fill, or a wait of the
+ * compute stream on a fill (the overlap of the write-up's section 3, as a
+ * timeline of the two streams). */
+typedef struct {
+    int32_t cls;      /* DLO_K_* */
+    int32_t block;    /* block index N; num_blocks = the next call's block 0 (DLO_PREFETCH_NEXT) */
+    int32_t stream;   /* 0: the compute stream passed to dlo_forward; 1: the handle's copy stream */
+    int32_t reserved; /* 0 */
+    double start_ms;  /* from the start of the forward on the compute stream */
+    double end_ms;
+} dlo_timeline_event;
+
+/* With DLO_PROFILE: the intervals of the most recent dlo_forward in the order
+ * they were enqueued.  Synchronises with that forward.  Writes the first
+ * min(cap, total) of them to the host array `out` (which may be null when cap
+ * is 0) and the total to *count; the caller owns `out`.  A handle created
+ * without DLO_PROFILE returns DLO_ERR_STATE; no forward yet gives *count = 0. */
+int dlo_get_timeline(dlo_handle* h, dlo_timeline_event* out, int32_t cap, int32_t* count);
+
 /* Test access to the slots: fills slot `slot` (0/1) with block `block` on the
  * copy stream using the handle's fill mechanism, waits, and copies `bytes`
  * bytes of the slot to host memory dst (bytes <= slot_bytes). */

@@ -44,7 +44,7 @@ EXPORTED = (
     "dlo_last_error", "dlo_status_string", "dlo_create", "dlo_forward", "dlo_forward_host", "dlo_synchronize",
     "dlo_get_stats", "dlo_get_kernel_times", "dlo_debug_fill_and_read", "dlo_destroy", "dlo_op_adaln",
     "dlo_op_ln_modulate", "dlo_op_linear", "dlo_op_attention", "dlo_op_shard_gather", "dlo_op_check",
-    "dlo_op_linear_noalloc", "dlo_forward_steps", "dlo_debug_fail_fill",
+    "dlo_op_linear_noalloc", "dlo_forward_steps", "dlo_debug_fail_fill", "dlo_get_timeline",
 )
 
 
@@ -73,6 +73,11 @@ class dlo_stats(ctypes.Structure):
                 ("h2d_zerocopy_gbs", ctypes.c_double)]
 
 
+class dlo_timeline_event(ctypes.Structure):
+    _fields_ = [("cls", ctypes.c_int32), ("block", ctypes.c_int32), ("stream", ctypes.c_int32),
+                ("reserved", ctypes.c_int32), ("start_ms", ctypes.c_double), ("end_ms", ctypes.c_double)]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -90,6 +95,7 @@ _SIGS = {
     "dlo_synchronize": [_c_p, _c_i32],
     "dlo_get_stats": [_c_p, ctypes.POINTER(dlo_stats)],
     "dlo_get_kernel_times": [_c_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_c_i64)],
+    "dlo_get_timeline": [_c_p, ctypes.c_void_p, _c_i32, ctypes.POINTER(_c_i32)],
     "dlo_debug_fill_and_read": [_c_p, _c_i32, _c_i32, _c_p, _c_i64],
     "dlo_debug_fail_fill": [_c_p, _c_i32],
     "dlo_destroy": [_c_p],
@@ -248,6 +254,17 @@ def dlo_get_kernel_times(handle: int) -> dict:
     ms, n = (ctypes.c_double * DLO_K_NUM)(), (_c_i64 * DLO_K_NUM)()
     _check(lib().dlo_get_kernel_times(handle, ms, n))
     return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_CLASSES)}
+
+
+def dlo_get_timeline(handle: int) -> list:
+    """The profiled intervals of the last forward, in enqueue order, as dicts
+    {kernel, block, stream ("compute" or "copy"), start_ms, end_ms}."""
+    n = _c_i32(0)
+    _check(lib().dlo_get_timeline(handle, None, 0, ctypes.byref(n)))
+    buf = (dlo_timeline_event * max(n.value, 1))()
+    _check(lib().dlo_get_timeline(handle, ctypes.cast(buf, ctypes.c_void_p), n.value, ctypes.byref(n)))
+    return [{"kernel": KERNEL_CLASSES[e.cls], "block": e.block, "stream": ("compute", "copy")[e.stream],
+             "start_ms": e.start_ms, "end_ms": e.end_ms} for e in buf[:n.value]]
 
 
 def dlo_debug_fill_and_read(handle: int, block: int, slot: int, dst, nbytes: int) -> None:

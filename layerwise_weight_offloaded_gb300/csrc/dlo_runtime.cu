@@ -159,7 +159,7 @@ struct ActMaps {
 };
 
 struct ProfEvent {
-    int cls;
+    int cls, block, on_copy;
     cudaEvent_t a, b;
 };
 
@@ -210,6 +210,7 @@ struct dlo_handle {
 
     std::vector<ProfEvent> prof_pool;
     size_t prof_used = 0;
+    cudaEvent_t prof_t0 = nullptr;  // DLO_PROFILE: start of the last forward on its compute stream
 
     dlo_stats st{};
 };
@@ -249,15 +250,17 @@ int issue_fill(dlo_handle* h, int b, uint16_t* dst, int mode) {
     return DLO_OK;
 }
 
-ProfEvent* prof_begin(dlo_handle* h, int cls, cudaStream_t s) {
+ProfEvent* prof_begin(dlo_handle* h, int cls, int block, cudaStream_t s) {
     if (!h->profile) return nullptr;
     if (h->prof_used == h->prof_pool.size()) {
-        ProfEvent e{cls, nullptr, nullptr};
+        ProfEvent e{cls, block, 0, nullptr, nullptr};
         if (cudaEventCreate(&e.a) != cudaSuccess || cudaEventCreate(&e.b) != cudaSuccess) return nullptr;
         h->prof_pool.push_back(e);
     }
     ProfEvent* e = &h->prof_pool[h->prof_used++];
     e->cls = cls;
+    e->block = block;
+    e->on_copy = s == h->copy;
     cudaEventRecord(e->a, s);
     return e;
 }
@@ -364,7 +367,7 @@ float* mod_buf(dlo_handle* h, int b) { return h->mod + (size_t)(b & 1) * h->req_
 int run_adaln(dlo_handle* h, int b, int slot, const float* cond, int R, cudaStream_t st) {
     const auto& sp = h->specs[b];
     const uint16_t* w = weights_base(h, b, h->resident ? 0 : slot);
-    ProfEvent* e = prof_begin(h, DLO_K_ADALN, st);
+    ProfEvent* e = prof_begin(h, DLO_K_ADALN, b, st);
     int rc = launch_adaln(w + h->off[b][DLO_P_ADA_W], w + h->off[b][DLO_P_ADA_B], cond, R, sp.cond_dim,
                           6 * sp.hidden, mod_buf(h, b), st);
     if (rc) return rc;
@@ -393,7 +396,7 @@ int run_block(dlo_handle* h, int b, int slot, float* x, const float* cond, int R
 
     if (!adaln_done && (rc = run_adaln(h, b, slot, cond, R, s))) return rc;
 
-    e = prof_begin(h, DLO_K_LN_MOD, s);
+    e = prof_begin(h, DLO_K_LN_MOD, b, s);
     if ((rc = launch_ln_modulate(x, mod + 0 * hd, mod + 1 * hd, ms, R, T, hd, h->u, s))) return rc;
     prof_end(e, s);
 
@@ -402,33 +405,33 @@ int run_block(dlo_handle* h, int b, int slot, float* x, const float* cond, int R
     a.M = M;
     a.T = T;
 
-    e = prof_begin(h, DLO_K_GEMM_QKV, s);
+    e = prof_begin(h, DLO_K_GEMM_QKV, b, s);
     a.epilogue = DLO_EPI_BIAS; a.N = 3 * hd; a.K = hd; a.bias = w + of[DLO_P_QKV_B]; a.out = h->qkv; a.gate = nullptr;
     a.out_map = &am.qkv_out;
     if ((rc = launch_gemm(am.u, bm.qkv, a, s, h->dev.num_sms))) return rc;
     prof_end(e, s);
 
-    e = prof_begin(h, DLO_K_ATTENTION, s);
+    e = prof_begin(h, DLO_K_ATTENTION, b, s);
     if ((rc = launch_attention(h->qkv, R, T, H, d, h->o, h->d_err, s))) return rc;
     prof_end(e, s);
 
-    e = prof_begin(h, DLO_K_GEMM_PROJ, s);
+    e = prof_begin(h, DLO_K_GEMM_PROJ, b, s);
     a.epilogue = DLO_EPI_GATED_RESIDUAL; a.N = hd; a.K = hd; a.bias = w + of[DLO_P_PROJ_B]; a.out = x;
     a.gate = mod + 2 * hd; a.gate_stride = ms; a.out_map = &am.x_out;
     if ((rc = launch_gemm(am.o, bm.proj, a, s, h->dev.num_sms))) return rc;
     prof_end(e, s);
 
-    e = prof_begin(h, DLO_K_LN_MOD, s);
+    e = prof_begin(h, DLO_K_LN_MOD, b, s);
     if ((rc = launch_ln_modulate(x, mod + 3 * hd, mod + 4 * hd, ms, R, T, hd, h->u, s))) return rc;
     prof_end(e, s);
 
-    e = prof_begin(h, DLO_K_GEMM_FC1, s);
+    e = prof_begin(h, DLO_K_GEMM_FC1, b, s);
     a.epilogue = DLO_EPI_BIAS_GELU; a.N = m; a.K = hd; a.bias = w + of[DLO_P_FC1_B]; a.out = h->g; a.gate = nullptr;
     a.out_map = &am.g_out;
     if ((rc = launch_gemm(am.u, bm.fc1, a, s, h->dev.num_sms))) return rc;
     prof_end(e, s);
 
-    e = prof_begin(h, DLO_K_GEMM_FC2, s);
+    e = prof_begin(h, DLO_K_GEMM_FC2, b, s);
     a.epilogue = DLO_EPI_GATED_RESIDUAL; a.N = hd; a.K = m; a.bias = w + of[DLO_P_FC2_B]; a.out = x;
     a.gate = mod + 5 * hd; a.gate_stride = ms; a.out_map = &am.x_out;
     if ((rc = launch_gemm(am.g, bm.fc2, a, s, h->dev.num_sms))) return rc;
@@ -470,6 +473,7 @@ void release(dlo_handle* h) {
     }
     if (h->start_ev) cudaEventDestroy(h->start_ev);
     if (h->done_ev) cudaEventDestroy(h->done_ev);
+    if (h->prof_t0) cudaEventDestroy(h->prof_t0);
     for (auto& e : h->prof_pool) {
         cudaEventDestroy(e.a);
         cudaEventDestroy(e.b);
@@ -566,6 +570,7 @@ int dlo_create(const dlo_block_spec* specs, int32_t num_blocks, int32_t dp_size,
     if ((e = cudaEventCreateWithFlags(&h->start_ev, cudaEventDisableTiming)) != cudaSuccess ||
         (e = cudaEventCreateWithFlags(&h->done_ev, cudaEventDisableTiming)) != cudaSuccess)
         return bail(cuda_error(e, "cudaEventCreate"));
+    if (h->profile && (e = cudaEventCreate(&h->prof_t0)) != cudaSuccess) return bail(cuda_error(e, "cudaEventCreate"));
     if ((e = cudaMalloc(&h->d_err, sizeof(int))) != cudaSuccess) return bail(cuda_error(e, "cudaMalloc(err)"));
     if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess) return bail(cuda_error(e, "cudaMemset"));
 
@@ -630,6 +635,8 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
     if ((rc = ensure_x_maps(h, x, (int64_t)R * T))) return fail(h, rc);
     h->prof_used = 0;
     cudaError_t e;
+    if (h->profile && (e = cudaEventRecord(h->prof_t0, s)) != cudaSuccess)
+        return fail(h, cuda_error(e, "cudaEventRecord(prof_t0)"));
 #define FWD_TRY(expr)                                            \
     do {                                                         \
         if ((e = (expr)) != cudaSuccess) return fail(h, cuda_error(e, #expr)); \
@@ -652,7 +659,7 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
         FWD_TRY(cudaStreamWaitEvent(h->copy, h->done_ev, 0));
         FWD_TRY(cudaStreamWaitEvent(s, h->done_ev, 0));
         if (!prefetched) {
-            ProfEvent* pe = prof_begin(h, DLO_K_FILL, h->copy);
+            ProfEvent* pe = prof_begin(h, DLO_K_FILL, 0, h->copy);
             if ((rc = issue_fill(h, 0, h->slot[slot_of(0)], h->fill_mode))) return fail(h, rc);
             prof_end(pe, h->copy);
             if ((rc = run_adaln(h, 0, slot_of(0), cond, R, h->copy))) return fail(h, rc);
@@ -667,14 +674,14 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
                 // freed[ns] marks the end of the last block that read slot ns: block
                 // N-1 of this call, or the previous call's last block.
                 if (N + 1 >= 2 || prefetched) FWD_TRY(cudaStreamWaitEvent(h->copy, h->freed[ns], 0));
-                ProfEvent* pe = prof_begin(h, DLO_K_FILL, h->copy);
+                ProfEvent* pe = prof_begin(h, DLO_K_FILL, N + 1, h->copy);
                 if ((rc = issue_fill(h, N + 1, h->slot[ns], h->fill_mode))) return fail(h, rc);
                 prof_end(pe, h->copy);
                 // the next block's modulation, beside this block's compute
                 if ((rc = run_adaln(h, N + 1, ns, cond, R, h->copy))) return fail(h, rc);
                 FWD_TRY(cudaEventRecord(h->filled[ns], h->copy));
             }
-            ProfEvent* pw = prof_begin(h, DLO_K_FILL_WAIT, s);
+            ProfEvent* pw = prof_begin(h, DLO_K_FILL_WAIT, N, s);
             FWD_TRY(cudaStreamWaitEvent(s, h->filled[slot], 0));
             prof_end(pw, s);
         }
@@ -691,11 +698,15 @@ int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t R, int32_t T
         // slot still serves block L-1); the next call skips that fill.
         const int nb = slot_of(h->L);
         FWD_TRY(cudaStreamWaitEvent(h->copy, h->freed[nb], 0));
+        ProfEvent* pe = prof_begin(h, DLO_K_FILL, h->L, h->copy);
         if ((rc = issue_fill(h, 0, h->slot[nb], h->fill_mode))) return fail(h, rc);
+        prof_end(pe, h->copy);
         FWD_TRY(cudaEventRecord(h->filled[nb], h->copy));
         // The forward completes on `stream` only once this fill has too: it runs
         // beside block L-1 and is the next call's first wait anyway.
+        ProfEvent* pw = prof_begin(h, DLO_K_FILL_WAIT, h->L, s);
         FWD_TRY(cudaStreamWaitEvent(s, h->filled[nb], 0));
+        prof_end(pw, s);
         h->next_base = nb;
         h->prefetched = true;
     } else {
@@ -792,6 +803,25 @@ int dlo_get_kernel_times(dlo_handle* h, double* ms, int64_t* launches) {
         if ((err = cudaEventElapsedTime(&t, e.a, e.b)) != cudaSuccess) return fail(h, cuda_error(err, "elapsed"));
         ms[e.cls] += t;
         launches[e.cls] += 1;
+    }
+    return DLO_OK;
+}
+
+int dlo_get_timeline(dlo_handle* h, dlo_timeline_event* out, int32_t cap, int32_t* count) {
+    if (!h || !count || (cap > 0 && !out)) return set_error(DLO_ERR_INVALID_ARG, "get_timeline: null pointer");
+    if (cap < 0) return set_error(DLO_ERR_INVALID_ARG, "get_timeline: cap must be >= 0");
+    if (!h->profile) return set_error(DLO_ERR_STATE, "get_timeline: handle created without DLO_PROFILE");
+    *count = (int32_t)h->prof_used;
+    const size_t n = std::min(h->prof_used, (size_t)cap);
+    for (size_t i = 0; i < n; ++i) {
+        const ProfEvent& e = h->prof_pool[i];
+        cudaError_t err = cudaEventSynchronize(e.b);
+        if (err != cudaSuccess) return fail(h, cuda_error(err, "get_timeline"));
+        float t0 = 0, t1 = 0;
+        if ((err = cudaEventElapsedTime(&t0, h->prof_t0, e.a)) != cudaSuccess ||
+            (err = cudaEventElapsedTime(&t1, h->prof_t0, e.b)) != cudaSuccess)
+            return fail(h, cuda_error(err, "elapsed"));
+        out[i] = dlo_timeline_event{e.cls, e.block, e.on_copy, 0, (double)t0, (double)t1};
     }
     return DLO_OK;
 }

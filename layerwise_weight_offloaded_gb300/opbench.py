@@ -7,7 +7,7 @@ shape and prints its CUDA-event time and rate: the mean over --reps
 back-to-back launches, best of --trials.  A ~1 ms device sleep is queued in
 front of each trial so that the host has enqueued every launch before the
 first one starts, and the host-side cost of a call (argument checks, tensor
-map encoding) stays out of the events.  This is the driver the ncu
+map encoding) stays out of the events.  This is the program the ncu
 summaries under profiles/ are captured from (`ncu -k regex:<kernel> -s W -c 1`
 skips the warm-up launches and captures the first timed one).
 

@@ -298,6 +298,59 @@ def test_profile_counts_every_kernel():
         run.close()
 
 
+
+@pytest.mark.parametrize("fill", [dlo.DLO_FILL_MEMCPY, dlo.DLO_FILL_ZEROCOPY])
+def test_timeline_shows_the_two_slot_schedule(fill):
+    """The per-interval timeline of a prefetched forward obeys the schedule of
+    the write-up's section 3: each stream runs its work in order; block N's
+    kernels start only after its slot fill ended; the fill of block N+1 starts
+    only after block N-1, the last reader of that slot, ended; and the
+    intervals add up to the per-class totals."""
+    cfg = synthetic.get_config("tiny")
+    L = cfg.blocks
+    specs = [spec_tuple(cfg)] * L
+    run = Run(specs, cfg.dp_size, flags=fill | dlo.DLO_PROFILE | dlo.DLO_PREFETCH_NEXT)
+    eps = 5e-3  # ms; event timestamps resolve to about a microsecond
+    try:
+        x, c = inputs((1, cfg.tokens, cfg.hidden, cfg.cond_dim), 0)
+        run.forward(x, c)
+        run.forward(x, c)  # the second call starts from the prefetched block 0
+        tl = dlo.dlo_get_timeline(run.h)
+        kt = dlo.dlo_get_kernel_times(run.h)
+        counts = {k: 0 for k in dlo.KERNEL_CLASSES}
+        for e in tl:
+            counts[e["kernel"]] += 1
+        assert counts == {"fill": L, "adaln": L, "ln_modulate": 2 * L, "gemm_qkv": L, "attention": L,
+                          "gemm_proj": L, "gemm_fc1": L, "gemm_fc2": L, "fill_wait": L + 1}
+        assert {k: v[1] for k, v in kt.items()} == counts
+        for k in dlo.KERNEL_CLASSES:
+            total = sum(e["end_ms"] - e["start_ms"] for e in tl if e["kernel"] == k)
+            assert total == pytest.approx(kt[k][0], rel=1e-3, abs=2e-3), k
+        for e in tl:
+            assert -eps <= e["start_ms"] <= e["end_ms"] + eps, e
+            on_copy = e["kernel"] == "fill" or (e["kernel"] == "adaln" and e["block"] > 0)
+            assert e["stream"] == ("copy" if on_copy else "compute"), e
+        for stream in ("compute", "copy"):
+            seq = [e for e in tl if e["stream"] == stream]
+            for a, b in zip(seq, seq[1:]):
+                assert b["start_ms"] >= a["end_ms"] - eps, (a, b)
+        fill = {e["block"]: e for e in tl if e["kernel"] == "fill"}
+        assert sorted(fill) == list(range(1, L + 1))  # block L: the next call's block 0
+        first = {}
+        last = {}
+        for e in tl:
+            if e["stream"] == "compute" and e["kernel"] != "fill_wait":
+                first.setdefault(e["block"], e["start_ms"])
+                last[e["block"]] = e["end_ms"]
+        for N in range(1, L):
+            assert first[N] >= fill[N]["end_ms"] - eps, N
+        for N in range(1, L + 1):
+            if N >= 2:
+                assert fill[N]["start_ms"] >= last[N - 2] - eps, N
+    finally:
+        run.close()
+
+
 def test_host_side_timeout_and_error_state():
     """A bounded host wait that expires reports DLO_ERR_TIMEOUT and fails the handle closed."""
     cfg = synthetic.get_config("tiny")

@@ -165,3 +165,41 @@ def test_pack_from_mmapped_flat_file_vs_oracle(tmp_path):
     np.zeros(10, np.uint16).tofile(short)
     with pytest.raises(ValueError):
         pack_from_flat_file(str(short), specs, dp, pin=False)
+
+
+def test_struct_layouts_and_constants_match_header(tmp_path):
+    """The ctypes mirrors of the header's structs and constants agree with what
+    a C compiler makes of include/dlo.h: sizes, field offsets and enum values."""
+    import ctypes
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"dlo_block_spec": dlo.dlo_block_spec, "dlo_stats": dlo.dlo_stats,
+               "dlo_timeline_event": dlo.dlo_timeline_event}
+    consts = [n for n in dir(dlo) if n.startswith("DLO_") and isinstance(getattr(dlo, n), int)]
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "dlo.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'printf("sizeof {name} %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'printf("offsetof {name}.{field} %zu\\n", offsetof({name}, {field}));')
+    for n in consts:
+        lines.append(f'printf("const {n} %lld\\n", (long long){n});')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True, capture_output=True, text=True)
+    got = dict(l.rsplit(" ", 1) for l in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                          text=True).stdout.splitlines())
+    want = {}
+    for name, cls in structs.items():
+        want[f"sizeof {name}"] = str(ctypes.sizeof(cls))
+        for field, _ in cls._fields_:
+            want[f"offsetof {name}.{field}"] = str(getattr(cls, field).offset)
+    for n in consts:
+        want[f"const {n}"] = str(getattr(dlo, n))
+    assert got == want
+    assert len(consts) >= 20
