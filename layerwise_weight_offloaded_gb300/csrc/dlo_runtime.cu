@@ -254,7 +254,11 @@ ProfEvent* prof_begin(dlo_handle* h, int cls, int block, cudaStream_t s) {
     if (!h->profile) return nullptr;
     if (h->prof_used == h->prof_pool.size()) {
         ProfEvent e{cls, block, 0, nullptr, nullptr};
-        if (cudaEventCreate(&e.a) != cudaSuccess || cudaEventCreate(&e.b) != cudaSuccess) return nullptr;
+        if (cudaEventCreate(&e.a) != cudaSuccess) return nullptr;
+        if (cudaEventCreate(&e.b) != cudaSuccess) {
+            cudaEventDestroy(e.a);
+            return nullptr;
+        }
         h->prof_pool.push_back(e);
     }
     ProfEvent* e = &h->prof_pool[h->prof_used++];
@@ -791,6 +795,8 @@ int dlo_get_stats(dlo_handle* h, dlo_stats* out) {
 int dlo_get_kernel_times(dlo_handle* h, double* ms, int64_t* launches) {
     if (!h || !ms || !launches) return set_error(DLO_ERR_INVALID_ARG, "get_kernel_times: null pointer");
     if (!h->profile) return set_error(DLO_ERR_STATE, "get_kernel_times: handle created without DLO_PROFILE");
+    // a failed forward leaves intervals without their end event
+    if (h->status) return set_error(DLO_ERR_STATE, "get_kernel_times: the handle is in an error state");
     for (int k = 0; k < DLO_K_NUM; ++k) {
         ms[k] = 0;
         launches[k] = 0;
@@ -811,6 +817,7 @@ int dlo_get_timeline(dlo_handle* h, dlo_timeline_event* out, int32_t cap, int32_
     if (!h || !count || (cap > 0 && !out)) return set_error(DLO_ERR_INVALID_ARG, "get_timeline: null pointer");
     if (cap < 0) return set_error(DLO_ERR_INVALID_ARG, "get_timeline: cap must be >= 0");
     if (!h->profile) return set_error(DLO_ERR_STATE, "get_timeline: handle created without DLO_PROFILE");
+    if (h->status) return set_error(DLO_ERR_STATE, "get_timeline: the handle is in an error state");
     *count = (int32_t)h->prof_used;
     const size_t n = std::min(h->prof_used, (size_t)cap);
     for (size_t i = 0; i < n; ++i) {
