@@ -21,6 +21,9 @@ Cases (M = R*T rows; weights [N, K] row-major):
     t2i-ln / video-ln / large-ln       LayerNorm+modulate, R*T x h = 4096x1536 /
                                        16384x5120 / 4x4096 x 8192
     t2i-adaln / large-adaln            adaLN GEMV, C=256: R=1, h=1536 / R=4, h=8192
+    t2i-gather / deep-gather           zero-copy slot fill of one block from its
+                                       pinned host shards: T2I block, dp=4 /
+                                       Deep block, dp=8
 """
 from __future__ import annotations
 
@@ -60,7 +63,12 @@ _ADALN = {
     "t2i-adaln": (1, 1536, 256),
     "large-adaln": (4, 8192, 256),
 }
-CASES = tuple(_ATTENTION) + tuple(_LINEAR) + tuple(_LN) + tuple(_ADALN)
+_GATHER = {
+    # name: (block spec (hidden, heads, mlp, cond_dim), dp)
+    "t2i-gather": ((1536, 24, 6144, 256), 4),
+    "deep-gather": ((3072, 24, 12288, 256), 8),
+}
+CASES = tuple(_ATTENTION) + tuple(_LINEAR) + tuple(_LN) + tuple(_ADALN) + tuple(_GATHER)
 
 
 def _bf16_bits(t: torch.Tensor) -> torch.Tensor:
@@ -103,6 +111,14 @@ def make_case(name: str, gen: torch.Generator):
         c = torch.randn(R, C, device=dev, generator=gen)
         mod = torch.empty(R, 6 * h, device=dev)
         return (lambda: B.dlo_op_adaln(W, b, c, R, C, 6 * h, mod)), 6.0 * h * C * 2 + R * 6 * h * 4, "GB/s"
+    if name in _GATHER:
+        spec, dp = _GATHER[name]
+        S = B.dlo_shard_numel(B.dlo_block_numel(spec), dp)
+        host = [torch.randint(-32768, 32767, (S,), dtype=torch.int16).pin_memory() for _ in range(dp)]
+        dst = torch.empty(dp * S, dtype=torch.int16, device=dev)
+        # the closure holds the pinned tensors themselves, so they outlive every launch;
+        # bytes over the host link (each read once) = bytes written to the slot
+        return (lambda: B.dlo_op_shard_gather(host, dp, S, dst)), 2.0 * dp * S, "GB/s"
     raise SystemExit(f"unknown case {name!r}; known: {', '.join(CASES)}")
 
 
