@@ -125,6 +125,12 @@ def test_invalid_arguments():
     assert L.dlo_create(None, 1, 1, None, 0, None) == dlo.DLO_ERR_INVALID_ARG
     assert L.dlo_forward(None, None, None, 1, 1, None) == dlo.DLO_ERR_INVALID_ARG
     assert L.dlo_destroy(None) == dlo.DLO_OK
+    n = ctypes.c_int32(-1)
+    assert L.dlo_get_timeline(None, None, 0, ctypes.byref(n)) == dlo.DLO_ERR_INVALID_ARG
+    assert n.value == -1  # nothing written on a rejected call
+    assert L.dlo_get_kernel_times(None, None, None) == dlo.DLO_ERR_INVALID_ARG
+    assert L.dlo_get_stats(None, None) == dlo.DLO_ERR_INVALID_ARG
+    assert L.dlo_synchronize(None, 0) == dlo.DLO_ERR_INVALID_ARG
     assert dlo.dlo_status_string(dlo.DLO_ERR_TIMEOUT) == "DLO_ERR_TIMEOUT"
 
 
