@@ -182,6 +182,36 @@ def test_forward_steps_equals_sequential_forwards():
         dlo.dlo_forward_steps(0, 0, 0, 1, 1, 1)
 
 
+
+@pytest.mark.parametrize("flags", [dlo.DLO_FILL_MEMCPY, dlo.DLO_FILL_ZEROCOPY | dlo.DLO_PREFETCH_NEXT])
+def test_forwards_on_switching_streams_equal_one_stream(flags):
+    """Back-to-back forwards issued on a different stream each, with no host
+    synchronisation between them, keep the order of the write-up's section 3
+    schedule: each call joins the previous one (slots, modulation buffers and
+    x are shared), so the result is bit-identical to the same calls on one
+    stream."""
+    cfg = synthetic.get_config("tiny")
+    specs = [spec_tuple(cfg)] * cfg.blocks
+    run = Run(specs, cfg.dp_size, flags=flags)
+    try:
+        x, c = inputs((2, cfg.tokens, cfg.hidden, cfg.cond_dim), 0)
+        cond = torch.from_numpy(c).cuda()
+        ref = torch.from_numpy(x).cuda()
+        for _ in range(3):
+            dlo.dlo_forward(run.h, ref, cond, 2, cfg.tokens, torch.cuda.current_stream())
+        dlo.dlo_synchronize(run.h, 120000)
+        got = torch.from_numpy(x).cuda()
+        streams = [torch.cuda.Stream() for _ in range(3)]
+        torch.cuda.synchronize()
+        for st in streams:
+            dlo.dlo_forward(run.h, got, cond, 2, cfg.tokens, st)
+        dlo.dlo_synchronize(run.h, 120000)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+    finally:
+        run.close()
+
+
 def test_pack_from_mmapped_flat_file(tmp_path):
     """Shards packed from a memory-mapped flat weight file equal shards packed
     from the parameter arrays, bit for bit, and stream the same forward."""
