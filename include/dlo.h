@@ -71,7 +71,8 @@ enum {
     DLO_FILL_ZEROCOPY = 2,  /* shard-gather kernel reading mapped pinned memory, 16-byte loads */
     DLO_FILL_MASK = 3,
     DLO_RESIDENT = 1 << 4,  /* copy every block to the device once (no streaming); for checks */
-    DLO_PROFILE = 1 << 5,   /* record CUDA events around every kernel (dlo_get_kernel_times) */
+    DLO_PROFILE = 1 << 5,   /* record CUDA events around every kernel, fill and fill wait
+                               (dlo_get_kernel_times, dlo_get_timeline) */
     DLO_PREFETCH_NEXT = 1 << 6 /* at the end of each forward, start filling block 0 of the next call
                                   into the slot block L-2 freed, so the next forward begins without
                                   waiting for it (a diffusion loop runs the forward once per step);
@@ -199,8 +200,14 @@ int dlo_create(const dlo_block_spec* specs, int32_t num_blocks, int32_t dp_size,
  * Asynchronous: the work is ordered after prior work on `stream` and the call
  * returns once it is enqueued (it may allocate activation scratch first).
  * Weight slots are refilled from the host shards on the handle's copy stream
- * while the previous block computes.  Concurrent calls on one handle from
- * several host threads are not supported. */
+ * while the previous block computes.  Consecutive calls on one handle are
+ * ordered even when issued on different streams: each call starts after the
+ * previous one has ended, since they share the slots and scratch.  Concurrent
+ * calls on one handle from several host threads are not supported.
+ * Errors: DLO_ERR_INVALID_ARG (null x or cond, R or T < 1), DLO_ERR_SHAPE
+ * (R > 65535 or R*T >= 2^31), DLO_ERR_ALIGNMENT (x not 16-byte or cond not
+ * 4-byte aligned) leave the handle usable; a failed CUDA call or allocation
+ * moves it to its error state. */
 int dlo_forward(dlo_handle* h, float* x, const float* cond, int32_t num_requests,
                 int32_t tokens_per_request, dlo_stream_t stream);
 
@@ -229,6 +236,8 @@ int dlo_forward_host(dlo_handle* h, float* x_host, const float* cond_host,
  * state), DLO_ERR_DEVICE_TIMEOUT if a kernel reported an expired wait. */
 int dlo_synchronize(dlo_handle* h, int32_t timeout_ms);
 
+/* Copies the handle's counters into the host struct *out.  Works in every
+ * state, including the error state; does not synchronise. */
 int dlo_get_stats(dlo_handle* h, dlo_stats* out);
 
 /* With DLO_PROFILE: per class (DLO_K_*), total device milliseconds and
