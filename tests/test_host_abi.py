@@ -209,3 +209,29 @@ def test_struct_layouts_and_constants_match_header(tmp_path):
         want[f"const {n}"] = str(getattr(dlo, n))
     assert got == want
     assert len(consts) >= 20
+
+
+def test_host_shards_separate_and_contiguous_vs_oracle():
+    """The shard allocations the runtime is given: separate buffers per rank,
+    or one buffer per block with the ranks back to back (one copy per fill).
+    Both hold the oracle's packing bit for bit; a parameter source of the
+    wrong size is refused."""
+    from layerwise_weight_offloaded_gb300.pinned import PinnedShards
+
+    specs = [(128, 2, 256, 32), (64, 1, 96, 16)]
+    dp = 3
+    src = lambda b, i, shape: synthetic.weight_bits(4, b, i, shape)
+    sep = PinnedShards(specs, dp, src, pin=False)
+    con = PinnedShards(specs, dp, src, contiguous=True, pin=False)
+    for b, (h, H, m, C) in enumerate(specs):
+        flat = np.concatenate([src(b, i, shape).reshape(-1) for i, (_, shape) in enumerate(dit.param_shapes(h, m, C))])
+        want = shards.pack(flat, dp)
+        S = want[0].size
+        base = con.ptrs[b * dp]
+        for r in range(dp):
+            assert np.array_equal(sep.shard_numpy(b, r), want[r])
+            assert np.array_equal(con.shard_numpy(b, r), want[r])
+            assert con.ptrs[b * dp + r] == base + 2 * r * S
+    assert sep.nbytes() == con.nbytes() == sum(dp * dlo.dlo_shard_numel(dlo.dlo_block_numel(s), dp) * 2 for s in specs)
+    with pytest.raises(ValueError):
+        PinnedShards(specs, dp, lambda b, i, shape: np.zeros(3, np.uint16), pin=False)
