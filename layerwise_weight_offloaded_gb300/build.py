@@ -49,8 +49,8 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def _compile(src: str, extra: list[str], verbose: bool) -> str:
-    obj = os.path.join(OBJ_DIR, src + ".o")
+def _compile(src: str, obj_dir: str, extra: list[str], verbose: bool) -> str:
+    obj = os.path.join(obj_dir, src + ".o")
     cmd = [nvcc(), *ARCH, *COMMON, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose:
         print(" ".join(cmd), flush=True)
@@ -63,23 +63,31 @@ def _compile(src: str, extra: list[str], verbose: bool) -> str:
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compiles every translation unit and links libdlo.so; returns its path."""
+    """Compiles every translation unit and links libdlo.so; returns its path.
+
+    Several processes may build at once (one per rank under torchrun): each
+    compiles into its own object directory and the finished library replaces
+    the old one atomically, so a reader never sees a partial file."""
     if not force and not ptxas_info and up_to_date():
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
-    os.makedirs(OBJ_DIR, exist_ok=True)
+    obj_dir = os.path.join(OBJ_DIR, str(os.getpid()))
+    os.makedirs(obj_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra, verbose or ptxas_info), SOURCES))
-    tmp = LIB + f".{os.getpid()}.tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs, "-cudart", "static", "-ldl", "-lpthread",
-           "-lrt"]
-    if verbose:
-        print(" ".join(cmd), flush=True)
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    try:
+        with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+            objs = list(ex.map(lambda s: _compile(s, obj_dir, extra, verbose or ptxas_info), SOURCES))
+        tmp = LIB + f".{os.getpid()}.tmp"
+        cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs, "-cudart", "static", "-ldl",
+               "-lpthread", "-lrt"]
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, LIB)
+    finally:
+        shutil.rmtree(obj_dir, ignore_errors=True)
     return LIB
 
 

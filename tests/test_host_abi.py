@@ -235,3 +235,22 @@ def test_host_shards_separate_and_contiguous_vs_oracle():
     assert sep.nbytes() == con.nbytes() == sum(dp * dlo.dlo_shard_numel(dlo.dlo_block_numel(s), dp) * 2 for s in specs)
     with pytest.raises(ValueError):
         PinnedShards(specs, dp, lambda b, i, shape: np.zeros(3, np.uint16), pin=False)
+
+
+def test_concurrent_builds_leave_a_loadable_library():
+    """Two processes building at once (as ranks under torchrun may) each use
+    their own object directory; the library left behind loads and exports
+    the ABI, and no object directory is left over."""
+    import subprocess
+    import sys
+    code = "from layerwise_weight_offloaded_gb300 import build; build.build(force=True)"
+    procs = [subprocess.Popen([sys.executable, "-c", code], cwd=ROOT, stdout=subprocess.PIPE,
+                              stderr=subprocess.PIPE, text=True) for _ in range(2)]
+    for p in procs:
+        out, err = p.communicate(timeout=600)
+        assert p.returncode == 0, err
+    import ctypes
+    L = ctypes.CDLL(dlo.LIB_PATH)
+    assert all(hasattr(L, s) for s in _declared_symbols())
+    obj_root = os.path.join(ROOT, "layerwise_weight_offloaded_gb300", "_build")
+    assert not os.path.isdir(obj_root) or not os.listdir(obj_root)
